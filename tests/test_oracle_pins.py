@@ -1,0 +1,346 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test pins one step of the MX-FP8 rule (OCP MX v1.0 conversion, E4M3
+elements, E8M0 scales, blocks of 32 in both directions as in pytorch/ao PR
+#1869 "triton kernel to cast to mx across dim0 and dim1", summary) to
+something independent: hand-worked bytes, a closed form, an independent
+library's encoder (ml_dtypes, torch's CPU float8 casts), an invariant, or a
+brute-force enumeration.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_block_scaled_dim0_gb300 import workloads as W
+
+ml_dtypes = pytest.importorskip("ml_dtypes")
+
+
+def np_bf16_values(bits):
+    """Independent bf16 decode: bf16 is the top half of an IEEE float32."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    with np.errstate(invalid="ignore"):
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+ALL_BF16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+FINITE_BF16 = ALL_BF16[((ALL_BF16 >> 7) & 0xFF) != 0xFF]
+
+
+# ---- hand-worked blocks ------------------------------------------------------
+
+def test_hand_worked_blocks_dim0_and_dim1(golden_blocks):
+    assert len(golden_blocks) >= 10
+    for name, _reading, scale, xs, qs in golden_blocks:
+        x = np.array(xs, dtype=np.uint16)
+        q0, s0 = oracle.cast_dim0(x.reshape(1, 32))
+        assert s0[0, 0] == scale, name
+        assert q0[0].tolist() == qs, name
+        q1, s1 = oracle.cast_dim1(x.reshape(32, 1))
+        assert s1[0, 0] == scale, name
+        assert q1[0].tolist() == qs, name
+
+
+def test_hand_worked_blocks_tiled_in_a_matrix(golden_blocks):
+    """The same blocks laid out as the blocks of a larger matrix: block j of
+    row i along dim0, and block i of column j along dim1 (catches index
+    mistakes in the multi-block loops)."""
+    cases = golden_blocks
+    n = len(cases)
+    X = np.zeros((n, 32 * n), np.uint16)
+    for i in range(n):
+        for j in range(n):
+            X[i, 32 * j:32 * j + 32] = cases[(i + j) % n][3]
+    q0, s0 = oracle.cast_dim0(X)
+    for i in range(n):
+        for j in range(n):
+            _, _, scale, _, qs = cases[(i + j) % n]
+            assert s0[i, j] == scale
+            assert q0[i, 32 * j:32 * j + 32].tolist() == qs
+    q1, s1 = oracle.cast_dim1(np.ascontiguousarray(X.T))
+    for i in range(n):
+        for j in range(n):
+            _, _, scale, _, qs = cases[(i + j) % n]
+            assert s1[i, j] == scale
+            assert q1[i, 32 * j:32 * j + 32].tolist() == qs
+
+
+# ---- scalar encodings --------------------------------------------------------
+
+def test_bf16_decode_all_patterns():
+    ref = np_bf16_values(ALL_BF16)
+    got = np.array([oracle.bf16_to_double(int(b)) for b in ALL_BF16])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_scale_closed_form_all_magnitudes():
+    """For a bf16 amax with biased exponent field E, floor(log2 amax) - 8
+    clamped and biased is max(E - 8, 0): subnormals and E <= 8 give 0."""
+    for sign in (0, 0x8000):
+        for b in range(0, 0x7F80):
+            v = np_bf16_values([b | sign])[0]
+            blk = np.zeros(32)
+            blk[b % 32] = v
+            E = b >> 7
+            assert oracle.block_scale(blk) == max(E - 8, 0), hex(b | sign)
+
+
+def test_scale_matches_e8m0_library_encoding():
+    """The scale byte of a block whose amax is in [2^(e+8), 2^(e+9)) is the
+    e8m0 encoding of 2^e (ml_dtypes float8_e8m0fnu)."""
+    for e in range(-127, 120):
+        ref = np.array([2.0 ** e]).astype(ml_dtypes.float8_e8m0fnu).view(np.uint8)[0]
+        for m in (1.0, 1.5, 1.9921875):
+            blk = np.zeros(32)
+            blk[3] = -m * 2.0 ** (e + 8)
+            assert oracle.block_scale(blk) == ref, (e, m)
+
+
+def test_scale_nan_inf_reading():
+    for bad in (np.nan, np.inf, -np.inf):
+        blk = np.ones(32)
+        blk[7] = bad
+        assert oracle.block_scale(blk) == 0xFF
+
+
+def _lib_e4m3_sat(v):
+    """Independent encoders: ml_dtypes and torch CPU, both round to nearest
+    even; neither saturates, so the input is clipped to +-448 first."""
+    c = np.clip(v, -448.0, 448.0)
+    a = c.astype(ml_dtypes.float8_e4m3fn).view(np.uint8)
+    t = torch.from_numpy(c.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return a, t
+
+
+def test_element_cast_exhaustive_vs_libraries():
+    """Every finite bf16 value, times 2^k for k in [-16, 16], through the
+    oracle's e4m3 encoder vs two independent library encoders."""
+    base = np_bf16_values(FINITE_BF16)
+    for k in range(-16, 17):
+        v = base * 2.0 ** k
+        got = oracle.e4m3_rne_sat_array(v)
+        a, t = _lib_e4m3_sat(v)
+        assert np.array_equal(got, a), k
+        assert np.array_equal(got, t), k
+
+
+def test_element_cast_every_bf16_every_scale():
+    """The element step as the rule applies it: for every finite bf16 x and
+    every finite scale byte s, e4m3(x * 2^(127 - s)) matches ml_dtypes."""
+    base = np_bf16_values(FINITE_BF16)
+    for s in range(0, 255):
+        v = base * 2.0 ** (127 - s)
+        got = oracle.e4m3_rne_sat_array(v)
+        ref = np.clip(v, -448.0, 448.0).astype(ml_dtypes.float8_e4m3fn).view(np.uint8)
+        assert np.array_equal(got, ref), s
+
+
+def test_e4m3_decode_all_bytes():
+    ref = np.arange(256, dtype=np.uint8).view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+    got = np.array([oracle.e4m3_to_double(b) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ---- directions --------------------------------------------------------------
+
+def small_matrix(kind, M, K, seed):
+    if kind == "spiky":
+        t = W.spiky(M, K, seed, scale_frac=0.05, zero_frac=0.05)
+    elif kind == "wide":
+        t = W.wide(M, K, seed, zero_frac=0.02)
+    else:
+        t = W.normal((M, K), seed)
+    return W.bf16_bits(t)
+
+
+@pytest.mark.parametrize("kind", ["spiky", "wide", "normal"])
+def test_dim1_equals_dim0_of_transpose(kind):
+    x = small_matrix(kind, 96, 160, 11)
+    q1, s1 = oracle.cast_dim1(x)
+    q0t, s0t = oracle.cast_dim0(np.ascontiguousarray(x.T))
+    assert np.array_equal(q1, q0t)
+    assert np.array_equal(s1, s0t)
+
+
+@pytest.mark.parametrize("kind", ["spiky", "wide"])
+def test_dequant_error_bound(kind):
+    """|x * 2^(127-s) - dq(q)| <= half an e4m3 ulp for unsaturated elements,
+    saturated elements only above 448 and only up to 512, and each block's
+    largest element lands in [256, 512) unless the scale is clamped at 0."""
+    x = small_matrix(kind, 64, 256, 5)
+    q, s = oracle.cast_dim0(x)
+    xv = np_bf16_values(x)
+    sv = np.repeat(s.astype(np.int64), 32, axis=1)
+    v = xv * np.exp2(127.0 - sv)
+    dq = q.view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+    a = np.abs(v)
+    assert a.max() < 512.0
+    with np.errstate(divide="ignore"):
+        ulp = np.where(a < 2.0 ** -6, 2.0 ** -9, np.exp2(np.floor(np.log2(np.maximum(a, 1e-300))) - 3))
+    unsat = a <= 448.0
+    assert np.all(np.abs(v - dq)[unsat] <= 0.5 * ulp[unsat])
+    assert np.all(np.abs(dq[~unsat]) == 448.0)
+    assert np.all(np.sign(dq[~unsat]) == np.sign(v[~unsat]))
+    amax = np.abs(xv.reshape(64, 8, 32)).max(axis=2)
+    vmax = amax * np.exp2(127.0 - s)
+    nz = (amax > 0) & (s > 0)
+    assert np.all((vmax[nz] >= 256.0) & (vmax[nz] < 512.0))
+
+
+# ---- blocked layout ----------------------------------------------------------
+
+def test_blocked_single_tile_positions():
+    """Brute force over one 128x4 tile: every (r, c) lands on its own byte,
+    and the positions follow the public description of the 1D block-scaling
+    factor layout: the tile is 32 rows of 16 bytes, and storage row i holds
+    rows i, i+32, i+64, i+96 of the scale matrix, 4 columns each."""
+    seen = {}
+    for r in range(128):
+        for c in range(4):
+            s = np.zeros((128, 4), np.uint8)
+            s[r, c] = 1
+            b = oracle.to_blocked(s)
+            assert b.size == 512 and b.sum() == 1
+            pos = int(np.argmax(b))
+            seen[(r, c)] = pos
+    assert sorted(seen.values()) == list(range(512))
+    storage = np.zeros((32, 16), dtype=object)
+    for (r, c), pos in seen.items():
+        storage[pos // 16, pos % 16] = (r, c)
+    for i in range(32):
+        for j in range(4):
+            for k in range(4):
+                assert storage[i, 4 * j + k] == (i + 32 * j, k)
+
+
+def test_blocked_hand_examples():
+    s = np.zeros((256, 8), np.uint8)
+    s[33, 2] = 7        # tile 0, storage row 1, group 1, column 2 -> 16+4+2
+    s[127, 3] = 9       # tile 0, last byte
+    s[128, 4] = 11      # tile (1, 1) -> 3 * 512
+    s[200, 1] = 13      # tile (1, 0) -> 2 * 512, r%128 = 72 -> 8*16 + 2*4 + 1
+    b = oracle.to_blocked(s)
+    assert b[22] == 7 and b[511] == 9 and b[1536] == 11 and b[1024 + 137] == 13
+    assert np.count_nonzero(b) == 4
+
+
+@pytest.mark.parametrize("R,C", [(1, 1), (130, 5), (128, 4), (300, 17), (1024, 160)])
+def test_blocked_padding_and_inverse(R, C):
+    rng = np.random.default_rng(R * 1000 + C)
+    s = rng.integers(1, 256, size=(R, C), dtype=np.uint8)
+    b = oracle.to_blocked(s)
+    assert b.size == (-(-R // 128) * 128) * (-(-C // 4) * 4)
+    assert np.count_nonzero(b) == R * C        # padding is zero, values kept
+    assert np.array_equal(oracle.from_blocked(b, R, C), s)
+    assert np.array_equal(np.sort(b[b != 0]), np.sort(s.ravel()))
+
+
+# ---- fused, grouped and 3D reductions ---------------------------------------
+
+def test_fused_blocked_is_blocked_of_plain():
+    x = small_matrix("spiky", 160, 224, 3)
+    q0, s0b, q1, s1b = oracle.cast_dim0_dim1_blocked(x)
+    p0, t0 = oracle.cast_dim0(x)
+    p1, t1 = oracle.cast_dim1(x)
+    assert np.array_equal(q0, p0) and np.array_equal(q1, p1)
+    assert np.array_equal(s0b, oracle.to_blocked(t0))
+    assert np.array_equal(s1b, oracle.to_blocked(t1))
+
+
+def test_grouped_single_group_is_ungrouped():
+    M, K = 160, 96
+    x = small_matrix("wide", M, K, 9)
+    q0, s0, r0, q1, s1, c1 = oracle.cast_grouped_m(x, np.array([M], np.int32))
+    p0, t0 = oracle.cast_dim0(x)
+    p1, t1 = oracle.cast_dim1(x)
+    assert np.array_equal(q0, p0) and np.array_equal(q1, p1)
+    b0, b1 = oracle.to_blocked(t0), oracle.to_blocked(t1)
+    assert np.array_equal(s0[:b0.size], b0) and not s0[b0.size:].any()
+    assert np.array_equal(s1[:b1.size], b1) and not s1[b1.size:].any()
+    assert r0.tolist() == [0, 256] and c1.tolist() == [0, 8]
+
+
+def test_grouped_multiples_of_128_dim0_is_ungrouped_blocked():
+    M, K = 512, 64
+    x = small_matrix("spiky", M, K, 4)
+    offs = np.array([128, 384, 384, 512], np.int32)   # includes an empty group
+    q0, s0, r0, q1, s1, c1 = oracle.cast_grouped_m(x, offs)
+    _, t0 = oracle.cast_dim0(x)
+    b0 = oracle.to_blocked(t0)
+    assert np.array_equal(s0[:b0.size], b0) and not s0[b0.size:].any()
+    p1, t1 = oracle.cast_dim1(x)
+    assert np.array_equal(q1, p1)
+    assert r0.tolist() == [0, 128, 384, 384, 512]
+    assert c1.tolist() == [0, 4, 12, 12, 16]
+    K128 = 128
+    lo = 0
+    for g, hi in enumerate(offs.tolist()):
+        if hi > lo:
+            want = oracle.to_blocked(t1[:, lo // 32:hi // 32])
+            at = K128 * c1[g]
+            assert np.array_equal(s1[at:at + want.size], want)
+        lo = hi
+
+
+def test_grouped_ragged_groups_match_standalone_casts():
+    """Each group equals the standalone cast of its own rows: dim0 scales in
+    blocked layout at the padded row offset, dim1 of the rows zero-padded to
+    a multiple of 32 at the padded column offset."""
+    M, K = 300, 160
+    x = small_matrix("wide", M, K, 21)
+    offs = np.array([1, 45, 45, 190, 300], np.int32)
+    q0, s0, r0, q1, s1, c1 = oracle.cast_grouped_m(x, offs)
+    p0, t0 = oracle.cast_dim0(x)
+    assert np.array_equal(q0, p0)
+    Kb4 = -(-(K // 32) // 4) * 4
+    K128 = -(-K // 128) * 128
+    lo = 0
+    covered0 = np.zeros(s0.size, bool)
+    covered1 = np.zeros(s1.size, bool)
+    for g, hi in enumerate(offs.tolist()):
+        m = hi - lo
+        assert r0[g + 1] - r0[g] == -(-m // 128) * 128
+        assert c1[g + 1] - c1[g] == -(-m // 128) * 4
+        if m:
+            b = oracle.to_blocked(t0[lo:hi])
+            at = int(r0[g]) * Kb4
+            assert np.array_equal(s0[at:at + b.size], b)
+            covered0[at:at + b.size] = True
+            mp = -(-m // 32) * 32
+            xg = np.zeros((mp, K), np.uint16)
+            xg[:m] = x[lo:hi]
+            gq, gs = oracle.cast_dim1(xg)
+            assert np.array_equal(q1[:, lo:hi], gq[:, :m])
+            b1 = oracle.to_blocked(gs)
+            at1 = K128 * int(c1[g])
+            assert np.array_equal(s1[at1:at1 + b1.size], b1)
+            covered1[at1:at1 + b1.size] = True
+        lo = hi
+    assert not s0[~covered0].any() and not s1[~covered1].any()
+
+
+@pytest.mark.parametrize("offs", [[5, 3, 10], [4, 12], [-1, 10], [10, 11]])
+def test_grouped_invalid_offsets(offs):
+    x = small_matrix("normal", 10, 32, 1)
+    with pytest.raises(ValueError):
+        oracle.cast_grouped_m(x, np.array(offs, np.int32))
+
+
+def test_3d_reductions():
+    E, N, K = 3, 64, 96
+    w = W.bf16_bits(W.experts(E, N, K, 17))
+    q1, s1 = oracle.cast_3d_dim1(w)
+    per = oracle.blocked_bytes(K, N // 32)
+    for e in range(E):
+        pq, ps = oracle.cast_dim1(w[e])
+        assert np.array_equal(q1[:, e * N:(e + 1) * N], pq)
+        assert np.array_equal(s1[e * per:(e + 1) * per], oracle.to_blocked(ps))
+    q1a, s1a = oracle.cast_3d_dim1(w[:1])
+    pq, ps = oracle.cast_dim1(w[0])
+    assert np.array_equal(q1a, pq) and np.array_equal(s1a, oracle.to_blocked(ps))
