@@ -1,0 +1,384 @@
+"""Benchmark of the fused MX-FP8 dim0 + dim1 cast with blocked scales.
+
+One step = one call of mx_cast_dim0_dim1 (one kernel launch) on the
+16384 x 16384 bf16 weight-like workload: read X once, write the row-major and
+column-major e4m3 copies and both e8m0 scale sets in 128x4 blocked layout.
+The metric is achieved HBM throughput: algorithmic bytes (2 B read + 1 + 1 B
+written per element, plus the padded blocked scales) per second of device
+time, and its fraction of the measured GB300 copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mx|reference]
+
+--impl reference times the CPU oracle (the plain C implementation used by the
+tests) on the host cores on a bounded sample of the same workload.  Under
+torchrun (N > 1) every rank casts its own copy of the workload on its own GPU
+(weak scaling, no collective on the data path); rank 0 prints the line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused MXFP8 dim0+dim1 cast HBM GB/s and fraction of GB300 HBM peak (1 GPU)"
+WORKLOAD = "square16384_weight"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["mxfp8_block_scaled_dim0_gb300/csrc/mx_cast.cu",
+                  "mxfp8_block_scaled_dim0_gb300/csrc/mx_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "mx_cast_fused_16384x16384.txt")
+
+
+def algorithmic_bytes(M, K):
+    """Bytes the fused cast must move: read X, write q0, q1 and both padded
+    blocked scale buffers."""
+    def blk(R, C):
+        return -(-R // 128) * 128 * (-(-C // 4) * 4)
+    return 2 * M * K + M * K + M * K + blk(M, K // 32) + blk(K, M // 32)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(units_scale=1.0):
+    """dram__bytes_read.sum + dram__bytes_write.sum per full launch from the
+    committed ncu summary, or None if absent or taken on other kernel code."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith(("#", " ", "|")):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_full_launch"]) * units_scale
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- clocks during the timed region ------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1].split()[0]))
+                    smax.append(float(parts[2].split()[0]))
+                except ValueError:
+                    continue
+                n += 1
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---- distributed plumbing (host logic; testable with gloo) ---------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, ws, device=None):
+    """Largest value over all ranks (identity when not distributed)."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_value(bytes_per_step, steps, n_ranks, max_elapsed_s):
+    """Whole-job GB/s: bytes every rank moved, over the slowest rank's time."""
+    return bytes_per_step * steps * n_ranks / max_elapsed_s / 1e9
+
+
+# ---- CPU oracle timing (the CPU baseline and the reference arm) ---------------
+
+def time_oracle(seconds_budget=12.0, rows_per_slab=512):
+    """Time the oracle's fused cast (dim0 + dim1 + blocked scales) on row slabs
+    of the workload until the budget is spent.  Returns (GB/s, rows, seconds)."""
+    import oracle
+    from mxfp8_block_scaled_dim0_gb300 import workloads as W
+    M, K = W.WORKLOADS[WORKLOAD].shape
+    x = W.bf16_bits(W.normal((rows_per_slab, K), W.WORKLOADS[WORKLOAD].seed, std=0.02))
+    oracle.library_path()
+    done_rows, t_used = 0, 0.0
+    while done_rows == 0 or (t_used < seconds_budget and done_rows < M):
+        t0 = time.perf_counter()
+        oracle.cast_dim0_dim1_blocked(x)
+        t_used += time.perf_counter() - t0
+        done_rows += rows_per_slab
+    gbs = algorithmic_bytes(done_rows, K) / t_used / 1e9
+    return gbs, done_rows, t_used
+
+
+def run_reference(args, budget_s=90.0):
+    """Reference arm: the oracle as it stands on the host cores.  Each step is
+    one fused cast of a bounded row slab of the workload, sized so that the
+    whole run (warm-up included) takes about budget_s seconds."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from mxfp8_block_scaled_dim0_gb300 import workloads as W
+    M, K = W.WORKLOADS[WORKLOAD].shape
+    seed = W.WORKLOADS[WORKLOAD].seed
+    calib = W.bf16_bits(W.normal((32, K), seed, std=0.02))
+    oracle.library_path()
+    t0 = time.perf_counter()
+    oracle.cast_dim0_dim1_blocked(calib)
+    t_row = (time.perf_counter() - t0) / 32
+    rows = int(budget_s / (args.steps + args.warmup) / t_row) // 32 * 32
+    rows = max(32, min(M, rows))
+    x = W.bf16_bits(W.normal((rows, K), seed, std=0.02))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.cast_dim0_dim1_blocked(x)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times)
+    rows_total = rows * len(times)
+    value = algorithmic_bytes(rows, K) * len(times) / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shape": [16384, 16384],
+                   "sample": "%d-row slab of the workload per step (bounded CPU sample)" % rows},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d rows x %d cols over %d steps" % (rows_total, K, len(times))},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- GPU arm ----------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import mxfp8_block_scaled_dim0_gb300 as mx
+    from mxfp8_block_scaled_dim0_gb300 import workloads as W
+    mx.library()
+
+    M, K = W.WORKLOADS[WORKLOAD].shape
+    nbytes = algorithmic_bytes(M, K)
+    stream = torch.cuda.current_stream(dev)
+
+    # Two input / output sets (each well above the 129 MB L2), alternated.
+    sets = []
+    for i in range(2):
+        x = W.normal((M, K), W.WORKLOADS[WORKLOAD].seed + 100 * i + rank, device=dev, std=0.02)
+        q0 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        q1 = torch.empty((K, M), dtype=torch.uint8, device=dev)
+        s0 = torch.empty(mx.mx_blocked_bytes(M, K // 32), dtype=torch.uint8, device=dev)
+        s1 = torch.empty(mx.mx_blocked_bytes(K, M // 32), dtype=torch.uint8, device=dev)
+        sets.append((x, q0, s0, q1, s1))
+
+    def step(i):
+        x, q0, s0, q1, s1 = sets[i & 1]
+        mx.mx_cast_dim0_dim1(x, q0, s0, q1, s1, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # timed region: K steps, an event pair around each launch and around all
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_beg = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if ws > 1 else int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0))
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.15)
+    t_beg.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    barrier(ws)
+    elapsed = t_beg.elapsed_time(t_end) / 1e3
+    per_launch = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    max_elapsed = max_over_ranks(elapsed, ws, dev)
+    value = whole_job_value(nbytes, args.steps, ws, max_elapsed)
+    avg_launch = sum(per_launch) / len(per_launch)
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / avg_launch / 1e9
+
+    # end-to-end through the public API with host buffers: pinned H2D of the
+    # input, the cast, D2H of all four outputs, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        x, q0, s0, q1, s1 = sets[0]
+        hx = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
+        hx.copy_(x)
+        hq0 = torch.empty_like(q0, device="cpu").pin_memory()
+        hq1 = torch.empty_like(q1, device="cpu").pin_memory()
+        hs0 = torch.empty_like(s0, device="cpu").pin_memory()
+        hs1 = torch.empty_like(s1, device="cpu").pin_memory()
+        dx = sets[1][0]
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            mx.mx_cast_dim0_dim1(dx, q0, s0, q1, s1, stream)
+            hq0.copy_(q0, non_blocking=True)
+            hs0.copy_(s0, non_blocking=True)
+            hq1.copy_(q1, non_blocking=True)
+            hs1.copy_(s1, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_el = max_over_ranks(a.elapsed_time(b) / 1e3, ws, dev)
+        h2d = 2 * M * K
+        d2h = q0.numel() + q1.numel() + s0.numel() + s1.numel()
+        e2e = {"value": whole_job_value(nbytes, args.e2e_steps, ws, e_el), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps, "ms_per_step": 1e3 * e_el / args.e2e_steps}
+        del hx, hq0, hq1, hs0, hs1
+
+    cpu = None
+    if rank == 0 and ws == 1 and args.cpu_seconds > 0:
+        gbs, rows, secs = time_oracle(seconds_budget=args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "first %d rows x %d cols of the workload (same value mix), %.1f s, "
+                         "fused dim0+dim1+blocked scales, single thread" % (rows, K, secs)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "shape": [M, K], "input": "bf16 N(0,1)*0.02",
+                       "bytes_per_step": nbytes,
+                       "l2": "inputs 512 MiB > 129 MB L2; two buffer sets alternated",
+                       "parallelism": "replicas" if ws > 1 else "single"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": measured_traffic(),
+                         "kernel": "mx_cast_kernel<fused2d>",
+                         "avg_launch_us": 1e6 * avg_launch},
+            "frac_of_peak": value / ws / peak,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["mx", "reference"], default="mx")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,152 @@
+/*
+ * mxfp8_cast.h -- C ABI of libmxfp8_cast.so: MX-FP8 (e4m3 elements, e8m0
+ * block scales, blocks of 32) quantisation of bf16 matrices on sm_103a.
+ *
+ * Conventions for every entry point below
+ *   - All data pointers are DEVICE pointers, allocated and owned by the
+ *     caller; the library allocates no device memory and keeps no pointer
+ *     after the call returns.
+ *   - Every pointer must be 16-byte aligned (int32 / int64 offset arrays:
+ *     4- / 8-byte aligned), tensors are dense row-major with no padding.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously; no call synchronises the device or reads
+ *     device memory on the host.  Results are valid once the stream has
+ *     executed the work.
+ *   - Return value: MX_OK, or a negative MX_ERR_* code.  Argument errors are
+ *     detected on the host before anything is enqueued (outputs untouched).
+ *     MX_ERR_CUDA means a CUDA call failed; mx_last_cuda_error() has its code.
+ *   - Calls that share an output buffer and run concurrently on the GPU race.
+ *
+ * The rule, per 32-element block (OCP Microscaling Formats v1.0 conversion
+ * with E4M3 elements and an E8M0 scale):
+ *   amax  = max |x_i|
+ *   scale byte s = clamp(floor(log2 amax) - 8, -127, 127) + 127; amax = 0
+ *                  gives s = 0; a block holding Inf or NaN gives s = 0xFF
+ *   q_i   = e4m3(x_i * 2^(127 - s)), round to nearest even, saturated to
+ *           +-448 (e4m3 NaN for every element of an Inf/NaN block)
+ * Directions (pytorch/ao PR #1869 "triton kernel to cast to mx across dim0
+ * and dim1", summary):
+ *   dim0: blocks along each row of X (M x K)    -> q0 (M x K) bytes
+ *   dim1: blocks along each column of X         -> q1 (K x M) bytes, the
+ *         row-major copy of X^T (X's column-major copy); q1[k][m] encodes
+ *         X[m][k]
+ * Blocked scale layout (the 128x4 layout of block-scaled GEMM scale factors;
+ * 128x4 is the granularity named in pytorch/ao PR #3416 "[mxfp8 moe training]
+ * parallelize along col blocks in scale blocked format kernel for groups
+ * along K"): a scale matrix S (R x C) is padded with zeros to
+ * ceil(R/128)*128 x ceil(C/4)*4, cut into 128x4 tiles stored one after
+ * another in row-major tile order (512 bytes each), and S[r][c] sits at byte
+ * (r%32)*16 + ((r%128)/32)*4 + c%4 of its tile.  Its size is
+ * mx_blocked_bytes(R, C).
+ */
+#ifndef MXFP8_CAST_H
+#define MXFP8_CAST_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MX_OK = 0,
+  MX_ERR_NULL = -1,    /* a required pointer is NULL */
+  MX_ERR_SHAPE = -2,   /* a size is zero, negative, too large or not a multiple of 32 */
+  MX_ERR_ALIGN = -3,   /* a pointer is not suitably aligned */
+  MX_ERR_CUDA = -4,    /* a CUDA call failed (see mx_last_cuda_error) */
+  MX_ERR_GROUPS = -5   /* invalid group count, or (device status) invalid offsets */
+};
+
+/* Fused dim0 + dim1 cast with both scale sets in blocked layout; one read of
+ * X.  Defined by pytorch/ao PR #1869 "triton kernel to cast to mx across dim0
+ * and dim1" (summary: read 32x32 tiles once, write the row-major and
+ * column-major casts and their scales from each tile; future work: outer
+ * tile 128, swizzled scales, coalesced writes).
+ *   x       bf16 (M x K), row-major                      [in]
+ *   M, K    M % 32 == 0, K % 32 == 0, 32 <= M, K <= 2^31 - 256
+ *   q0      M x K bytes, e4m3, dim0                      [out]
+ *   s0_blk  mx_blocked_bytes(M, K/32) bytes, e8m0        [out]
+ *   q1      K x M bytes, e4m3, dim1                      [out]
+ *   s1_blk  mx_blocked_bytes(K, M/32) bytes, e8m0        [out]
+ * Padding bytes of the blocked buffers are written as zero. */
+int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, void* q1,
+                      void* s1_blk, void* stream);
+
+/* dim1 cast only (the column-major copy and its blocked scales), as split out
+ * of the fused kernel in the same pull request's follow-up (dim1 logic in its
+ * own kernel).  Arguments as in mx_cast_dim0_dim1. */
+int mx_cast_dim1(const void* x, int64_t M, int64_t K, void* q1, void* s1_blk, void* stream);
+
+/* Standalone conversion of a plain scale matrix to the blocked layout, the
+ * operation of the scale-blocking kernels in pytorch/ao PR #3416 (Changes
+ * list) and PR #2990 (perf analysis, scale swizzle kernels).
+ *   s    R x C bytes, row-major, any alignment           [in]
+ *   R, C >= 1, R <= 65535 * 128
+ *   out  mx_blocked_bytes(R, C) bytes, 16-byte aligned   [out] */
+int mx_scales_to_blocked(const void* s, int64_t R, int64_t C, void* out, void* stream);
+
+/* Fused dim0 + dim1 cast of MoE activations with groups along M (pytorch/ao
+ * PR #2990 "[mxfp8 moe training] add compile support": groups of rows given
+ * by offsets; scale buffers sized by the bound rows + groups * 128 so that no
+ * device-to-host read is needed).
+ *   x            bf16 (M x K)                                   [in]
+ *   M, K         M >= 1, K % 32 == 0, M, K <= 2^31 - 256
+ *   offs         G int32 cumulative group ends (group g = rows
+ *                [offs[g-1], offs[g]), offs[-1] = 0; offs[G-1] == M;
+ *                empty groups allowed), device memory           [in]
+ *   G            >= 1 (else MX_ERR_GROUPS)
+ *   q0           M x K bytes: the ungrouped dim0 cast           [out]
+ *   s0_blk       mx_grouped_m_scale_bytes(M, K, G, 0) bytes: group g's scale
+ *                rows in blocked layout on their own, starting at row
+ *                s0_row_offs[g] (byte s0_row_offs[g] * ceil4(K/32)) [out]
+ *   s0_row_offs  G + 1 int64: sum over h < g of ceil(m_h/128)*128 [out]
+ *   q1           K x M bytes: group g is the dim1 cast of its own rows
+ *                (blocks of 32 start at the group's first row; the last
+ *                block may be partial and counts missing rows as zero),
+ *                in columns [offs[g-1], offs[g])                [out]
+ *   s1_blk       mx_grouped_m_scale_bytes(M, K, G, 1) bytes: group g's
+ *                (K x ceil(m_g/32)) scales in blocked layout on their own at
+ *                byte ceil128(K) * s1_col_offs[g]                [out]
+ *   s1_col_offs  G + 1 int64: sum over h < g of ceil(m_h/128)*4 [out]
+ *   status       one int32, device memory: 0, or MX_ERR_GROUPS if the offsets
+ *                are invalid (then nothing else is written)     [out]
+ * Every byte of both scale buffers is written (padding zero). */
+int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, int32_t G,
+                      void* q0, void* s0_blk, int64_t* s0_row_offs, void* q1, void* s1_blk,
+                      int64_t* s1_col_offs, int32_t* status, void* stream);
+
+/* dim1 cast of 3D expert weights (pytorch/ao PR #2990, perf analysis: cast
+ * the (E, N, K) weights as the reshaped 2D matrix (E*N, K) with the dim1
+ * kernel, scales per expert).
+ *   w       bf16 (E, N, K)                                       [in]
+ *   E >= 1, N % 32 == 0, K % 32 == 0, E*N and K <= 2^31 - 256
+ *   q1      K x (E*N) bytes: the dim1 cast of the (E*N, K) matrix;
+ *           expert e owns columns [e*N, (e+1)*N)                  [out]
+ *   s1_blk  mx_3d_scale_bytes(E, N, K) bytes: expert e's (K x N/32)
+ *           scales in blocked layout at byte e * mx_blocked_bytes(K, N/32)
+ *                                                                 [out] */
+int mx_cast_3d_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q1, void* s1_blk,
+                    void* stream);
+
+/* Size helpers (host only, no CUDA calls).  Return -1 for invalid sizes. */
+int64_t mx_blocked_bytes(int64_t R, int64_t C);
+/* dim 0: (M + 128*G) * ceil4(K/32); dim 1: ceil128(K) * (ceil(M/32) + 4*G). */
+int64_t mx_grouped_m_scale_bytes(int64_t M, int64_t K, int32_t G, int32_t dim);
+int64_t mx_3d_scale_bytes(int64_t E, int64_t N, int64_t K);
+
+/* Text for an MX_* code (static storage). */
+const char* mx_strerror(int code);
+
+/* cudaError_t value of the last failed CUDA call made by this thread. */
+int mx_last_cuda_error(void);
+
+/* Device watchdog: every wait inside the kernels is bounded; a CTA that gives
+ * up sets a device word.  Returns that word (0 or 1) after synchronising the
+ * current device, clearing it if `clear` is non-zero, or MX_ERR_CUDA. */
+int mx_watchdog(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_CAST_H */

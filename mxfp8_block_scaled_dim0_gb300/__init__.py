@@ -1,0 +1,252 @@
+"""MX-FP8 casts of bf16 matrices on sm_103a (GB300): Python binding.
+
+Thin ctypes layer over the C ABI of ``libmxfp8_cast.so`` (declared in
+``include/mxfp8_cast.h``).  Functions named like the C entry points take torch
+tensors, check their shapes, and pass raw device pointers plus the current
+CUDA stream; every step of the cast runs in the library's CUDA kernels.  There
+is no CPU fallback: if the library has not been built, importing the binding
+raises.
+
+Convenience wrappers (``cast_dim0_dim1``, ``cast_dim1``, ``cast_grouped_m``,
+``cast_3d_dim1``, ``scales_to_blocked``) allocate outputs with torch and call
+the same entry points.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmxfp8_cast.so")
+
+MX_OK = 0
+MX_ERR_NULL = -1
+MX_ERR_SHAPE = -2
+MX_ERR_ALIGN = -3
+MX_ERR_CUDA = -4
+MX_ERR_GROUPS = -5
+
+# Every function the header declares, for load checks.
+ABI_SYMBOLS = (
+    "mx_cast_dim0_dim1", "mx_cast_dim1", "mx_scales_to_blocked", "mx_cast_grouped_m",
+    "mx_cast_3d_dim1", "mx_blocked_bytes", "mx_grouped_m_scale_bytes", "mx_3d_scale_bytes",
+    "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
+)
+
+
+class MXError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        msg = "%s failed: %s (%d)" % (where, _lib().mx_strerror(code).decode(), code)
+        if code == MX_ERR_CUDA:
+            msg += " [cudaError %d]" % _lib().mx_last_cuda_error()
+        super().__init__(msg)
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                "libmxfp8_cast.so is not built (expected at %s); build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` or "
+                "`python -m mxfp8_block_scaled_dim0_gb300.build`" % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        sig = {
+            "mx_cast_dim0_dim1": ([P, I64, I64, P, P, P, P, P], ctypes.c_int),
+            "mx_cast_dim1": ([P, I64, I64, P, P, P], ctypes.c_int),
+            "mx_scales_to_blocked": ([P, I64, I64, P, P], ctypes.c_int),
+            "mx_cast_grouped_m": ([P, I64, I64, P, I32, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "mx_cast_3d_dim1": ([P, I64, I64, I64, P, P, P], ctypes.c_int),
+            "mx_blocked_bytes": ([I64, I64], I64),
+            "mx_grouped_m_scale_bytes": ([I64, I64, I32, I32], I64),
+            "mx_3d_scale_bytes": ([I64, I64, I64], I64),
+            "mx_strerror": ([ctypes.c_int], ctypes.c_char_p),
+            "mx_last_cuda_error": ([], ctypes.c_int),
+            "mx_watchdog": ([ctypes.c_int], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = lib
+    return _LIB
+
+
+def library():
+    """The loaded ctypes library (raises ImportError if it is not built)."""
+    return _lib()
+
+
+# ---- marshalling helpers ----------------------------------------------------
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev_tensor(t, name, nbytes=None, itemsize=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if itemsize is not None and t.element_size() != itemsize:
+        raise TypeError("%s must have %d-byte elements" % (name, itemsize))
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError("%s holds %d bytes, needs %d" % (name, t.numel() * t.element_size(), nbytes))
+    return t
+
+
+def _check(rc, where):
+    if rc != MX_OK:
+        raise MXError(rc, where)
+
+
+# ---- sizes ------------------------------------------------------------------
+
+def mx_blocked_bytes(R, C):
+    return int(_lib().mx_blocked_bytes(R, C))
+
+
+def mx_grouped_m_scale_bytes(M, K, G, dim):
+    return int(_lib().mx_grouped_m_scale_bytes(M, K, G, dim))
+
+
+def mx_3d_scale_bytes(E, N, K):
+    return int(_lib().mx_3d_scale_bytes(E, N, K))
+
+
+# ---- entry points (same names as the C ABI) ----------------------------------
+
+def mx_cast_dim0_dim1(x, q0, s0_blk, q1, s1_blk, stream=None):
+    """Fused dim0 + dim1 cast of bf16 x (M x K) into caller buffers."""
+    _dev_tensor(x, "x", itemsize=2)
+    M, K = x.shape
+    _dev_tensor(q0, "q0", M * K, 1)
+    _dev_tensor(q1, "q1", M * K, 1)
+    _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), 1)
+    _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), 1)
+    _check(_lib().mx_cast_dim0_dim1(_ptr(x), M, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
+                                    _ptr(s1_blk), _stream(stream)), "mx_cast_dim0_dim1")
+
+
+def mx_cast_dim1(x, q1, s1_blk, stream=None):
+    _dev_tensor(x, "x", itemsize=2)
+    M, K = x.shape
+    _dev_tensor(q1, "q1", M * K, 1)
+    _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), 1)
+    _check(_lib().mx_cast_dim1(_ptr(x), M, K, _ptr(q1), _ptr(s1_blk), _stream(stream)),
+           "mx_cast_dim1")
+
+
+def mx_scales_to_blocked(s, out, stream=None):
+    _dev_tensor(s, "s", itemsize=1)
+    R, C = s.shape
+    _dev_tensor(out, "out", mx_blocked_bytes(R, C), 1)
+    _check(_lib().mx_scales_to_blocked(_ptr(s), R, C, _ptr(out), _stream(stream)),
+           "mx_scales_to_blocked")
+
+
+def mx_cast_grouped_m(x, offs, q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs, status,
+                      stream=None):
+    _dev_tensor(x, "x", itemsize=2)
+    M, K = x.shape
+    _dev_tensor(offs, "offs", itemsize=4)
+    G = offs.numel()
+    _dev_tensor(q0, "q0", M * K, 1)
+    _dev_tensor(q1, "q1", M * K, 1)
+    if G >= 1:
+        _dev_tensor(s0_blk, "s0_blk", mx_grouped_m_scale_bytes(M, K, G, 0), 1)
+        _dev_tensor(s1_blk, "s1_blk", mx_grouped_m_scale_bytes(M, K, G, 1), 1)
+    _dev_tensor(s0_row_offs, "s0_row_offs", 8 * (G + 1), 8)
+    _dev_tensor(s1_col_offs, "s1_col_offs", 8 * (G + 1), 8)
+    _dev_tensor(status, "status", 4, 4)
+    _check(_lib().mx_cast_grouped_m(_ptr(x), M, K, _ptr(offs), G, _ptr(q0), _ptr(s0_blk),
+                                    _ptr(s0_row_offs), _ptr(q1), _ptr(s1_blk), _ptr(s1_col_offs),
+                                    _ptr(status), _stream(stream)), "mx_cast_grouped_m")
+
+
+def mx_cast_3d_dim1(w, q1, s1_blk, stream=None):
+    _dev_tensor(w, "w", itemsize=2)
+    E, N, K = w.shape
+    _dev_tensor(q1, "q1", E * N * K, 1)
+    _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), 1)
+    _check(_lib().mx_cast_3d_dim1(_ptr(w), E, N, K, _ptr(q1), _ptr(s1_blk), _stream(stream)),
+           "mx_cast_3d_dim1")
+
+
+def mx_watchdog(clear=True):
+    rc = _lib().mx_watchdog(1 if clear else 0)
+    if rc < 0:
+        raise MXError(rc, "mx_watchdog")
+    return rc
+
+
+# ---- allocating wrappers ------------------------------------------------------
+
+def _u8(n, device):
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def cast_dim0_dim1(x, stream=None):
+    """Returns (q0 (M,K), s0_blk, q1 (K,M), s1_blk) as uint8 tensors."""
+    M, K = x.shape
+    q0 = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    q1 = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    s0 = _u8(mx_blocked_bytes(M, K // 32), x.device)
+    s1 = _u8(mx_blocked_bytes(K, M // 32), x.device)
+    mx_cast_dim0_dim1(x, q0, s0, q1, s1, stream)
+    return q0, s0, q1, s1
+
+
+def cast_dim1(x, stream=None):
+    M, K = x.shape
+    q1 = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    s1 = _u8(mx_blocked_bytes(K, M // 32), x.device)
+    mx_cast_dim1(x, q1, s1, stream)
+    return q1, s1
+
+
+def scales_to_blocked(s, stream=None):
+    R, C = s.shape
+    out = _u8(mx_blocked_bytes(R, C), s.device)
+    mx_scales_to_blocked(s, out, stream)
+    return out
+
+
+def cast_grouped_m(x, offs, stream=None):
+    """offs: int32 CUDA tensor of cumulative group ends.  Returns
+    (q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs, status)."""
+    M, K = x.shape
+    G = offs.numel()
+    dev = x.device
+    q0 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    q1 = torch.empty((K, M), dtype=torch.uint8, device=dev)
+    s0 = _u8(mx_grouped_m_scale_bytes(M, K, G, 0), dev)
+    s1 = _u8(mx_grouped_m_scale_bytes(M, K, G, 1), dev)
+    r0 = torch.empty(G + 1, dtype=torch.int64, device=dev)
+    c1 = torch.empty(G + 1, dtype=torch.int64, device=dev)
+    st = torch.empty(1, dtype=torch.int32, device=dev)
+    mx_cast_grouped_m(x, offs, q0, s0, r0, q1, s1, c1, st, stream)
+    return q0, s0, r0, q1, s1, c1, st
+
+
+def cast_3d_dim1(w, stream=None):
+    E, N, K = w.shape
+    q1 = torch.empty((K, E * N), dtype=torch.uint8, device=w.device)
+    s1 = _u8(mx_3d_scale_bytes(E, N, K), w.device)
+    mx_cast_3d_dim1(w, q1, s1, stream)
+    return q1, s1

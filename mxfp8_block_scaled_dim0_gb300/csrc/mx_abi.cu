@@ -1,0 +1,234 @@
+// mx_abi.cu -- the C ABI (include/mxfp8_cast.h): argument checks, TMA
+// descriptor encoding and kernel launches.  No device allocation, no device
+// synchronisation, no host reads of device memory on any cast path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "mx_kernels.h"
+#include "mxfp8_cast.h"
+
+namespace {
+
+thread_local int t_last_cuda = 0;
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 256;   // TMA coordinates are int32
+
+int cuda_fail(int code) {
+  t_last_cuda = code;
+  return MX_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so that the
+// library needs no link-time dependency on libcuda.
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// 2D tiled map: inner dimension `inner` (elements), `outer` rows `stride`
+// bytes apart, box `bin` x `bout`, 128-byte swizzle.
+int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+              uint64_t outer, uint64_t stride, uint32_t bin, uint32_t bout,
+              CUtensorMapL2promotion l2) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return cuda_fail(static_cast<int>(cudaErrorNotSupported));
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {stride};
+  const cuuint32_t box[2] = {bin, bout};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(static_cast<int>(cudaErrorInvalidValue));
+  return MX_OK;
+}
+
+// Descriptors for X (M x K bf16), q0 (M x K bytes) and q1 (K x M bytes, as
+// its even and odd rows).  q0 / q1 may be null (not used by the call).
+int encode_cast_maps(mx::CastMaps* maps, const void* x, int64_t M, int64_t K, const void* q0,
+                     const void* q1) {
+  int rc = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, 128,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc) return rc;
+  if (q0) {
+    rc = encode_2d(&maps->q0, CU_TENSOR_MAP_DATA_TYPE_UINT8, q0, K, M, K, 128, 128,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (rc) return rc;
+  } else {
+    maps->q0 = maps->x;   // never dereferenced
+  }
+  if (q1) {
+    rc = encode_2d(&maps->q1e, CU_TENSOR_MAP_DATA_TYPE_UINT8, q1, M, K / 2, 2 * M, 128, 64,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (rc) return rc;
+    rc = encode_2d(&maps->q1o, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<const uint8_t*>(q1) + M,
+                   M, K / 2, 2 * M, 128, 64, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (rc) return rc;
+  } else {
+    maps->q1e = maps->x;
+    maps->q1o = maps->x;
+  }
+  return MX_OK;
+}
+
+int current_sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(static_cast<int>(e));
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(static_cast<int>(e));
+  return MX_OK;
+}
+
+int check_2d_shape(int64_t M, int64_t K) {
+  if (M < 32 || K < 32 || M > kMaxDim || K > kMaxDim) return MX_ERR_SHAPE;
+  if (M % 32 != 0 || K % 32 != 0) return MX_ERR_SHAPE;
+  return MX_OK;
+}
+
+int launch_rc(int rc) { return rc ? cuda_fail(rc) : MX_OK; }
+
+}  // namespace
+
+extern "C" {
+
+int64_t mx_blocked_bytes(int64_t R, int64_t C) {
+  if (R < 0 || C < 0) return -1;
+  return cdiv(R, 128) * 128 * cdiv(C, 4) * 4;
+}
+
+int64_t mx_grouped_m_scale_bytes(int64_t M, int64_t K, int32_t G, int32_t dim) {
+  if (M < 0 || K < 0 || G < 1 || (dim != 0 && dim != 1)) return -1;
+  if (dim == 0) return (M + 128 * static_cast<int64_t>(G)) * cdiv(K / 32, 4) * 4;
+  return cdiv(K, 128) * 128 * (cdiv(M, 32) + 4 * static_cast<int64_t>(G));
+}
+
+int64_t mx_3d_scale_bytes(int64_t E, int64_t N, int64_t K) {
+  if (E < 0 || N < 0 || K < 0) return -1;
+  return E * mx_blocked_bytes(K, N / 32);
+}
+
+const char* mx_strerror(int code) {
+  switch (code) {
+    case MX_OK: return "ok";
+    case MX_ERR_NULL: return "null pointer argument";
+    case MX_ERR_SHAPE: return "invalid shape (zero, too large, or not a multiple of 32)";
+    case MX_ERR_ALIGN: return "misaligned pointer (16-byte alignment required)";
+    case MX_ERR_CUDA: return "CUDA call failed (see mx_last_cuda_error)";
+    case MX_ERR_GROUPS: return "invalid group count or group offsets";
+    default: return "unknown error";
+  }
+}
+
+int mx_last_cuda_error(void) { return t_last_cuda; }
+
+int mx_watchdog(int clear) {
+  int v = 0;
+  int rc = mx::read_watchdog(&v, clear != 0);
+  if (rc) return cuda_fail(rc);
+  return v;
+}
+
+int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, void* q1,
+                      void* s1_blk, void* stream) {
+  if (!x || !q0 || !s0_blk || !q1 || !s1_blk) return MX_ERR_NULL;
+  if (int rc = check_2d_shape(M, K)) return rc;
+  if (!aligned(x, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16) || !aligned(q1, 16) ||
+      !aligned(s1_blk, 16))
+    return MX_ERR_ALIGN;
+  mx::CastMaps maps;
+  if (int rc = encode_cast_maps(&maps, x, M, K, q0, q1)) return rc;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  return launch_rc(mx::launch_cast_2d(maps, M, K, true, s0_blk, s1_blk, sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int mx_cast_dim1(const void* x, int64_t M, int64_t K, void* q1, void* s1_blk, void* stream) {
+  if (!x || !q1 || !s1_blk) return MX_ERR_NULL;
+  if (int rc = check_2d_shape(M, K)) return rc;
+  if (!aligned(x, 16) || !aligned(q1, 16) || !aligned(s1_blk, 16)) return MX_ERR_ALIGN;
+  mx::CastMaps maps;
+  if (int rc = encode_cast_maps(&maps, x, M, K, nullptr, q1)) return rc;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  return launch_rc(mx::launch_cast_2d(maps, M, K, false, nullptr, s1_blk, sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int mx_scales_to_blocked(const void* s, int64_t R, int64_t C, void* out, void* stream) {
+  if (!s || !out) return MX_ERR_NULL;
+  if (R < 1 || C < 1 || R > int64_t{65535} * 128 || C > kMaxDim) return MX_ERR_SHAPE;
+  if (!aligned(out, 16)) return MX_ERR_ALIGN;
+  return launch_rc(mx::launch_scales_to_blocked(static_cast<const uint8_t*>(s), R, C,
+                                                static_cast<uint8_t*>(out),
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, int32_t G,
+                      void* q0, void* s0_blk, int64_t* s0_row_offs, void* q1, void* s1_blk,
+                      int64_t* s1_col_offs, int32_t* status, void* stream) {
+  if (!x || !offs || !q0 || !s0_blk || !s0_row_offs || !q1 || !s1_blk || !s1_col_offs || !status)
+    return MX_ERR_NULL;
+  if (G < 1) return MX_ERR_GROUPS;
+  if (M < 1 || K < 32 || M > kMaxDim || K > kMaxDim || K % 32 != 0) return MX_ERR_SHAPE;
+  if (M + 128 * static_cast<int64_t>(G) > kMaxDim) return MX_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16) || !aligned(q1, 16) ||
+      !aligned(s1_blk, 16) || !aligned(offs, 4) || !aligned(s0_row_offs, 8) ||
+      !aligned(s1_col_offs, 8) || !aligned(status, 4))
+    return MX_ERR_ALIGN;
+  mx::CastMaps maps;
+  // q1 is written with plain stores (group starts are not 16-byte aligned).
+  if (int rc = encode_cast_maps(&maps, x, M, K, q0, nullptr)) return rc;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (int rc = mx::launch_group_offsets(offs, G, M, s0_row_offs, s1_col_offs, status, st))
+    return cuda_fail(rc);
+  return launch_rc(mx::launch_cast_grouped(maps, M, K, offs, G, q1, s0_blk, s0_row_offs, s1_blk,
+                                           status, sms, st));
+}
+
+int mx_cast_3d_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q1, void* s1_blk,
+                    void* stream) {
+  if (!w || !q1 || !s1_blk) return MX_ERR_NULL;
+  if (E < 1 || N < 32 || N % 32 != 0 || K < 32 || K % 32 != 0) return MX_ERR_SHAPE;
+  if (N > kMaxDim || E > kMaxDim / N || K > kMaxDim) return MX_ERR_SHAPE;
+  if (!aligned(w, 16) || !aligned(q1, 16) || !aligned(s1_blk, 16)) return MX_ERR_ALIGN;
+  const int64_t M = E * N;
+  mx::CastMaps maps;
+  if (int rc = encode_cast_maps(&maps, w, M, K, nullptr, q1)) return rc;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (N % 128 != 0) {
+    // Scales are scattered byte by byte in this case; the padding of each
+    // expert's blocked matrix is cleared first.
+    cudaError_t e = cudaMemsetAsync(s1_blk, 0, static_cast<size_t>(mx_3d_scale_bytes(E, N, K)), st);
+    if (e != cudaSuccess) return cuda_fail(static_cast<int>(e));
+  }
+  return launch_rc(mx::launch_cast_experts(maps, E, N, K, s1_blk, sms, st));
+}
+
+}  // extern "C"

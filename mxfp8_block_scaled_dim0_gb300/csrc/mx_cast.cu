@@ -1,0 +1,563 @@
+// mx_cast.cu -- persistent, warp-specialised MX-FP8 cast kernels for sm_103a.
+//
+// One pass over a bf16 matrix X (M x K, row-major) writes
+//   q0  (M x K)  e4m3, blocks of 32 along rows     ("dim0")
+//   q1  (K x M)  e4m3, blocks of 32 along columns  ("dim1", X's column-major copy)
+// and the e8m0 scales of both, already in the 128x4 blocked layout that
+// block-scaled GEMMs read.  This is the fused cast of pytorch/ao PR #1869
+// "triton kernel to cast to mx across dim0 and dim1" (summary: read each tile
+// once, write both copies and their scales from it), with the future-work
+// items of that summary built in: an outer tile of 128, scales written
+// swizzled, and coalesced writes of the column-major copy.  The grouped-M and
+// 3D variants follow pytorch/ao PR #2990 "[mxfp8 moe training] add compile
+// support" (padding bound rows + groups*128 with no host sync; 3D weights cast
+// as the reshaped 2D matrix).
+//
+// Tile = 128 rows x 128 columns of X.  Such a tile yields exactly one 512-byte
+// 128x4 blocked scale tile per direction, so the swizzle costs nothing.
+//
+// CTA roles (one CTA per SM, persistent over tiles):
+//   warps 0-7  compute: dim0 and dim1 block maxima, scales, e4m3 packing,
+//              into swizzled shared-memory staging tiles
+//   warp 8     producer: TMA loads of the bf16 tile (two 64-column halves,
+//              128B swizzle) into a kStages-deep ring
+//   warp 9     storer: TMA stores of the staged fp8 tiles and bulk copies of
+//              the 512-byte scale tiles
+// Every wait is bounded (see mbar_wait); on time-out the CTA raises an abort
+// flag, stops, drains its own bulk copies and reports through a device word.
+#include <cuda_runtime.h>
+
+#include "mx_common.cuh"
+#include "mx_kernels.h"
+
+namespace mx {
+
+// Device-side watchdog word: set when any CTA gave up waiting.
+__device__ int g_watchdog = 0;
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kHalfBytes = 128 * 128;      // 64 bf16 columns x 128 rows
+constexpr int kInBytes = 2 * kHalfBytes;    // one bf16 tile
+constexpr int kQBytes = 128 * 128;          // one e4m3 tile
+constexpr int kQ1Half = 64 * 128;           // even / odd columns of a q1 tile
+constexpr int kScaleTile = 512;
+constexpr int kStages = 4;
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kThreads = kComputeThreads + 64;
+constexpr int kProducerWarp = kComputeWarps;
+constexpr int kStoreWarp = kComputeWarps + 1;
+
+// Shared-memory layout, offsets from a 1024-byte aligned base (the 128B
+// swizzle pattern repeats every 1024 bytes).
+constexpr int kOffIn = 0;
+constexpr int kOffQ0 = kOffIn + kStages * kInBytes;
+constexpr int kOffQ1 = kOffQ0 + 2 * kQBytes;
+constexpr int kOffS0 = kOffQ1 + 2 * kQBytes;
+constexpr int kOffS1 = kOffS0 + 2 * kScaleTile;
+constexpr int kOffBar = kOffS1 + 2 * kScaleTile;
+constexpr int kNumBars = 2 * kStages + 6;
+constexpr int kOffFlag = kOffBar + kNumBars * 8;
+constexpr int kSmemUsed = kOffFlag + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+enum Mode : int { kModeFused2D = 0, kModeDim1 = 1, kModeExperts = 2, kModeGrouped = 3 };
+
+struct Tile {
+  int32_t m0;       // first row of X
+  int32_t k0;       // first column of X
+  int32_t rows;     // rows of the tile that belong to it (grouped mode), else 128
+  int32_t pad_;
+  uint8_t* s0_dst;  // 512-byte blocked tile for dim0 scales
+  uint8_t* s1_dst;  // 512-byte blocked tile for dim1 scales (null: scattered)
+};
+
+struct Params {
+  int64_t M, K;
+  int32_t n_mt, n_kt;       // tiles along M and K
+  int64_t n_tiles;          // 2D / 3D modes
+  uint8_t* s0;
+  uint8_t* s1;
+  uint8_t* q1;              // grouped mode: plain stores of q1
+  // experts (3D)
+  int64_t N;                // rows per expert
+  int64_t s1_expert_bytes;  // blk(K, N/32)
+  int32_t s1_scatter;       // N % 128 != 0: scales written byte by byte
+  int32_t nb4;              // ceil4(N / 32)
+  // grouped
+  const int32_t* offs;
+  const int64_t* row_offs;  // s0_row_offs (G + 1)
+  const int32_t* status;
+  int32_t G;
+  int32_t k128;             // ceil128(K)
+};
+
+__device__ __forceinline__ int64_t grouped_tiles(const Params& p) {
+  return (p.row_offs[p.G] >> 7) * p.n_kt;
+}
+
+template <int kMode>
+__device__ __forceinline__ Tile get_tile(const Params& p, int64_t t) {
+  Tile T;
+  T.pad_ = 0;
+  if (kMode == kModeGrouped) {
+    const int64_t R = t / p.n_kt;                  // padded tile-row
+    const int32_t tk = static_cast<int32_t>(t - R * p.n_kt);
+    const int64_t v = R << 7;
+    int lo = 0, hi = p.G;                          // row_offs[lo] <= v < row_offs[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.row_offs[mid] <= v) lo = mid; else hi = mid;
+    }
+    const int g = lo;
+    const int64_t t_in_g = R - (p.row_offs[g] >> 7);
+    const int64_t n_tg = (p.row_offs[g + 1] - p.row_offs[g]) >> 7;
+    const int64_t start = g ? p.offs[g - 1] : 0;
+    const int64_t m0 = start + (t_in_g << 7);
+    const int64_t left = static_cast<int64_t>(p.offs[g]) - m0;
+    T.m0 = static_cast<int32_t>(m0);
+    T.k0 = tk * kTile;
+    T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
+    T.s0_dst = p.s0 + (R * p.n_kt + tk) * kScaleTile;
+    T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (p.row_offs[g] >> 5) +
+               (tk * n_tg + t_in_g) * kScaleTile;
+  } else {
+    const int32_t tm = static_cast<int32_t>(t / p.n_kt);
+    const int32_t tk = static_cast<int32_t>(t - static_cast<int64_t>(tm) * p.n_kt);
+    T.m0 = tm * kTile;
+    T.k0 = tk * kTile;
+    T.rows = kTile;
+    T.s0_dst = p.s0 ? p.s0 + t * kScaleTile : nullptr;
+    if (kMode == kModeExperts) {
+      if (p.s1_scatter) {
+        T.s1_dst = nullptr;
+      } else {
+        const int64_t e = T.m0 / p.N;
+        const int64_t nt = (T.m0 - e * p.N) >> 7;
+        T.s1_dst = p.s1 + e * p.s1_expert_bytes + (tk * (p.N >> 7) + nt) * kScaleTile;
+      }
+    } else {
+      T.s1_dst = p.s1 + (static_cast<int64_t>(tk) * p.n_mt + tm) * kScaleTile;
+    }
+  }
+  return T;
+}
+
+// ---- compute units ----------------------------------------------------------
+
+// dim0 unit: one 32-element block (row `row`, block `b` of 4) of the tile.
+// Reads four 16-byte chunks of the 128B-swizzled input, writes 32 e4m3 bytes
+// to the swizzled q0 staging tile and one scale byte to the staging scale
+// tile.  Rows at or beyond `rows` get scale 0 (padding of a group).
+__device__ __forceinline__ void dim0_unit(const uint8_t* in, uint8_t* q0s, uint8_t* sc0,
+                                          int row, int b, int rows) {
+  const int sw = row & 7;
+  const uint8_t* src = in + (b >> 1) * kHalfBytes + row * 128;
+  uint4 v[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int q = ((b & 1) << 2) + h;
+    v[h] = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
+  }
+  uint32_t a0 = absmax2(absmax2(v[0].x, v[0].y), absmax2(v[0].z, v[0].w));
+  uint32_t a1 = absmax2(absmax2(v[1].x, v[1].y), absmax2(v[1].z, v[1].w));
+  uint32_t a2 = absmax2(absmax2(v[2].x, v[2].y), absmax2(v[2].z, v[2].w));
+  uint32_t a3 = absmax2(absmax2(v[3].x, v[3].y), absmax2(v[3].z, v[3].w));
+  const uint32_t a = absmax2(absmax2(a0, a1), absmax2(a2, a3));
+  const uint32_t lo = mag_lo(a), hi = mag_hi(a);
+  uint32_t sbyte;
+  float m;
+  mx_scale(lo > hi ? lo : hi, sbyte, m);
+
+  uint4 o0, o1;
+  o0.x = e4m3x4(bf_lo(v[0].x), bf_hi(v[0].x), bf_lo(v[0].y), bf_hi(v[0].y), m);
+  o0.y = e4m3x4(bf_lo(v[0].z), bf_hi(v[0].z), bf_lo(v[0].w), bf_hi(v[0].w), m);
+  o0.z = e4m3x4(bf_lo(v[1].x), bf_hi(v[1].x), bf_lo(v[1].y), bf_hi(v[1].y), m);
+  o0.w = e4m3x4(bf_lo(v[1].z), bf_hi(v[1].z), bf_lo(v[1].w), bf_hi(v[1].w), m);
+  o1.x = e4m3x4(bf_lo(v[2].x), bf_hi(v[2].x), bf_lo(v[2].y), bf_hi(v[2].y), m);
+  o1.y = e4m3x4(bf_lo(v[2].z), bf_hi(v[2].z), bf_lo(v[2].w), bf_hi(v[2].w), m);
+  o1.z = e4m3x4(bf_lo(v[3].x), bf_hi(v[3].x), bf_lo(v[3].y), bf_hi(v[3].y), m);
+  o1.w = e4m3x4(bf_lo(v[3].z), bf_hi(v[3].z), bf_lo(v[3].w), bf_hi(v[3].w), m);
+  uint8_t* dst = q0s + row * 128;
+  *reinterpret_cast<uint4*>(dst + (((2 * b) ^ sw) << 4)) = o0;
+  *reinterpret_cast<uint4*>(dst + (((2 * b + 1) ^ sw) << 4)) = o1;
+  sc0[blocked_in_tile(row, b)] = static_cast<uint8_t>(row < rows ? sbyte : 0u);
+}
+
+// Four consecutive rows of one column of a dim1 unit -> four e4m3 bytes.
+#define MX_COL4_LO(w, j, m) e4m3x4(bf_lo(w[j]), bf_lo(w[j + 1]), bf_lo(w[j + 2]), bf_lo(w[j + 3]), m)
+#define MX_COL4_HI(w, j, m) e4m3x4(bf_hi(w[j]), bf_hi(w[j + 1]), bf_hi(w[j + 2]), bf_hi(w[j + 3]), m)
+
+// dim1 unit: column pair p (columns 2p, 2p+1 of the tile), rows 32*mb ..
+// 32*mb+31.  Reads one 4-byte word per row (a warp reads whole 128-byte rows,
+// conflict-free under the swizzle), writes 32 e4m3 bytes per column into the
+// even / odd halves of the q1 staging tile (row p of each half) and the two
+// scale bytes.  Rows at or beyond `rows` are treated as zero (grouped mode).
+// Returns the two scale bytes (even column in bits 0-7, odd in 8-15).
+template <bool kMask>
+__device__ __forceinline__ uint32_t dim1_unit(const uint8_t* in, uint8_t* q1s, uint8_t* sc1,
+                                              int p, int mb, int rows) {
+  const int wd = p & 31;
+  const int ch = wd >> 2;
+  const uint8_t* src = in + (p >> 5) * kHalfBytes + (mb * 32) * 128 + (wd & 3) * 4;
+  uint32_t w[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    w[j] = *reinterpret_cast<const uint32_t*>(src + j * 128 + ((ch ^ (j & 7)) << 4));
+  if (kMask) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (mb * 32 + j >= rows) w[j] = 0u;
+  }
+  uint32_t t[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = absmax2(w[2 * j], w[2 * j + 1]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t[j] = absmax2(t[2 * j], t[2 * j + 1]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t[j] = absmax2(t[2 * j], t[2 * j + 1]);
+  const uint32_t a = absmax2(absmax2(t[0], t[1]), absmax2(t[2], t[3]));
+  uint32_t se, so;
+  float me, mo;
+  mx_scale(mag_lo(a), se, me);
+  mx_scale(mag_hi(a), so, mo);
+
+  uint4 e0, e1, o0, o1;
+  e0.x = MX_COL4_LO(w, 0, me);  e0.y = MX_COL4_LO(w, 4, me);
+  e0.z = MX_COL4_LO(w, 8, me);  e0.w = MX_COL4_LO(w, 12, me);
+  e1.x = MX_COL4_LO(w, 16, me); e1.y = MX_COL4_LO(w, 20, me);
+  e1.z = MX_COL4_LO(w, 24, me); e1.w = MX_COL4_LO(w, 28, me);
+  o0.x = MX_COL4_HI(w, 0, mo);  o0.y = MX_COL4_HI(w, 4, mo);
+  o0.z = MX_COL4_HI(w, 8, mo);  o0.w = MX_COL4_HI(w, 12, mo);
+  o1.x = MX_COL4_HI(w, 16, mo); o1.y = MX_COL4_HI(w, 20, mo);
+  o1.z = MX_COL4_HI(w, 24, mo); o1.w = MX_COL4_HI(w, 28, mo);
+  const int sw = p & 7;
+  uint8_t* de = q1s + p * 128;
+  uint8_t* dodd = q1s + kQ1Half + p * 128;
+  *reinterpret_cast<uint4*>(de + (((2 * mb) ^ sw) << 4)) = e0;
+  *reinterpret_cast<uint4*>(de + (((2 * mb + 1) ^ sw) << 4)) = e1;
+  *reinterpret_cast<uint4*>(dodd + (((2 * mb) ^ sw) << 4)) = o0;
+  *reinterpret_cast<uint4*>(dodd + (((2 * mb + 1) ^ sw) << 4)) = o1;
+  sc1[blocked_in_tile(2 * p, mb)] = static_cast<uint8_t>(se);
+  sc1[blocked_in_tile(2 * p + 1, mb)] = static_cast<uint8_t>(so);
+  return se | (so << 8);
+}
+#undef MX_COL4_LO
+#undef MX_COL4_HI
+
+// Grouped mode: copy the staged q1 tile (128 columns of X = 128 rows of q1,
+// `len` valid bytes each) to q1 at row k0 + c, column m0.  Group starts need
+// not be aligned, so each warp writes one q1 row per step as 4-byte words
+// (128 contiguous bytes per step), with byte stores at the ragged ends.
+__device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* q1, int64_t M, int64_t K,
+                                            int m0, int k0, int len, int warp, int lane) {
+  for (int c = warp; c < kTile; c += kComputeWarps) {
+    const int64_t kk = static_cast<int64_t>(k0) + c;
+    if (kk >= K) break;
+    const int64_t A = kk * M + m0;                 // byte offset of the row segment
+    const int al = static_cast<int>(A & 3);
+    const int64_t w0 = A >> 2;
+    const int nw = static_cast<int>(((A + len + 3) >> 2) - w0);
+    const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
+    const int sw = (c >> 1) & 7;
+    for (int j = lane; j < nw; j += 32) {
+      const int l0 = al ? j - 1 : j;               // staging word holding the first byte
+      uint32_t x0 = 0u, x1 = 0u;
+      if (l0 >= 0 && l0 < 32)
+        x0 = *reinterpret_cast<const uint32_t*>(srow + (((l0 >> 2) ^ sw) << 4) + (l0 & 3) * 4);
+      if (al && l0 + 1 < 32)
+        x1 = *reinterpret_cast<const uint32_t*>(srow + ((((l0 + 1) >> 2) ^ sw) << 4) +
+                                                ((l0 + 1) & 3) * 4);
+      const uint32_t val = al ? __funnelshift_r(x0, x1, 8 * (4 - al)) : x0;
+      const int o = 4 * j - al;                    // local offset of the word's byte 0
+      const int b_lo = o < 0 ? -o : 0;
+      const int b_hi = (len - o) < 4 ? (len - o) : 4;
+      uint8_t* g = q1 + ((w0 + j) << 2);
+      if (b_lo == 0 && b_hi == 4) {
+        *reinterpret_cast<uint32_t*>(g) = val;
+      } else {
+        for (int b = b_lo; b < b_hi; ++b) g[b] = static_cast<uint8_t>(val >> (8 * b));
+      }
+    }
+  }
+}
+
+// ---- the kernel -------------------------------------------------------------
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_cast_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q0,
+                   const __grid_constant__ CUtensorMap tm_q1e,
+                   const __grid_constant__ CUtensorMap tm_q1o, const Params p) {
+  constexpr bool kDim0 = (kMode == kModeFused2D || kMode == kModeGrouped);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = bars;                  // [kStages] TMA landed
+  uint64_t* empty = bars + kStages;       // [kStages] compute done reading
+  uint64_t* sfull = bars + 2 * kStages;   // [2] staging written
+  uint64_t* sempty = sfull + 2;           // [2] staging read by the bulk engine
+  uint64_t* qstaged = sfull + 4;          // [2] grouped: q1 staging complete
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int64_t n_tiles;
+  if (kMode == kModeGrouped) {
+    if (*p.status != 0) return;           // invalid group offsets: write nothing
+    n_tiles = grouped_tiles(p);
+  } else {
+    n_tiles = p.n_tiles;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kComputeWarps);
+    }
+    for (int o = 0; o < 2; ++o) {
+      mbar_init(&sfull[o], kComputeWarps);
+      mbar_init(&sempty[o], 1);
+      mbar_init(&qstaged[o], kComputeWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int64_t first = blockIdx.x;
+  const int64_t step = gridDim.x;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_x);
+      int64_t it = 0;
+      for (int64_t t = first; t < n_tiles; t += step, ++it) {
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
+        const Tile T = get_tile<kMode>(p, t);
+        uint8_t* dst = smem + kOffIn + s * kInBytes;
+        mbar_arrive_expect_tx(&full[s], kInBytes);
+        tma_load_2d(dst, &tm_x, T.k0, T.m0, &full[s]);
+        tma_load_2d(dst + kHalfBytes, &tm_x, T.k0 + 64, T.m0, &full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kStoreWarp) {
+    if (lane == 0) {
+      if (kDim0) prefetch_tmap(&tm_q0);
+      if (kMode != kModeGrouped) {
+        prefetch_tmap(&tm_q1e);
+        prefetch_tmap(&tm_q1o);
+      }
+      int64_t it = 0;
+      for (int64_t t = first; t < n_tiles; t += step, ++it) {
+        const int o = static_cast<int>(it & 1);
+        const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
+        if (!mbar_wait(&sfull[o], ph, abort_flag)) break;
+        const Tile T = get_tile<kMode>(p, t);
+        if (kDim0) {
+          tma_store_2d(&tm_q0, T.k0, T.m0, smem + kOffQ0 + o * kQBytes);
+          bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
+        }
+        if (kMode != kModeGrouped) {
+          tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes);
+          tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes + kQ1Half);
+        }
+        if (T.s1_dst) bulk_store(T.s1_dst, smem + kOffS1 + o * kScaleTile, kScaleTile);
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(&sempty[o]);
+      }
+      bulk_wait<0>();
+    }
+    __syncwarp();
+  } else {
+    // compute warps
+    int64_t it = 0;
+    for (int64_t t = first; t < n_tiles; t += step, ++it) {
+      const int s = static_cast<int>(it % kStages);
+      const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+      const int o = static_cast<int>(it & 1);
+      const uint32_t oph = static_cast<uint32_t>((it >> 1) & 1);
+      bool ok = mbar_wait(&full[s], ph, abort_flag);
+      ok = ok && mbar_wait(&sempty[o], oph ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+
+      const Tile T = get_tile<kMode>(p, t);
+      const uint8_t* in = smem + kOffIn + s * kInBytes;
+      uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
+      uint8_t* sc1 = smem + kOffS1 + o * kScaleTile;
+      if (kDim0) {
+        uint8_t* q0s = smem + kOffQ0 + o * kQBytes;
+        uint8_t* sc0 = smem + kOffS0 + o * kScaleTile;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int row = (2 * warp + u) * 8 + (lane & 7);
+          dim0_unit(in, q0s, sc0, row, lane >> 3, T.rows);
+        }
+      }
+      const int mb = warp >> 1;
+      const int pcol = (warp & 1) * 32 + lane;
+      uint32_t sb;
+      if (kMode == kModeGrouped && T.rows < kTile)
+        sb = dim1_unit<true>(in, q1s, sc1, pcol, mb, T.rows);
+      else
+        sb = dim1_unit<false>(in, q1s, sc1, pcol, mb, T.rows);
+
+      if (kMode == kModeExperts && T.s1_dst == nullptr) {
+        // 3D weights with N % 128 != 0: a tile can straddle two experts, so
+        // each scale byte goes straight to its expert's blocked matrix.
+        const int64_t mbg = (static_cast<int64_t>(T.m0) >> 5) + mb;
+        if ((mbg << 5) < p.M) {
+          const int64_t e = (mbg << 5) / p.N;
+          const int64_t col = mbg - e * (p.N >> 5);
+          uint8_t* base = p.s1 + e * p.s1_expert_bytes;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t kk = T.k0 + 2 * pcol + h;
+            if (kk < p.K) base[blocked_offset(kk, col, p.nb4)] = static_cast<uint8_t>(sb >> (8 * h));
+          }
+        }
+      }
+
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);     // input stage may be refilled
+
+      if (kMode == kModeGrouped) {
+        // All compute warps must have staged q1 before any copies it out.  An
+        // mbarrier (bounded wait) rather than bar.sync, so that a CTA whose
+        // other warps stopped on the abort flag cannot hang here.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qstaged[o]);
+        const bool staged = mbar_wait(&qstaged[o], oph, abort_flag);
+        if (!__all_sync(0xffffffffu, staged)) break;
+        copy_out_q1(q1s, p.q1, p.M, p.K, T.m0, T.k0, T.rows, warp, lane);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfull[o]);
+    }
+
+    if (kMode == kModeGrouped) {
+      // Zero the scale buffers' tails beyond the last group's padded end.
+      const int64_t kb4 = static_cast<int64_t>(p.n_kt) * 4;
+      const int64_t s0_beg = p.row_offs[p.G] * kb4;
+      const int64_t s0_end = (p.M + 128 * static_cast<int64_t>(p.G)) * kb4;
+      const int64_t s1_beg = static_cast<int64_t>(p.k128) * (p.row_offs[p.G] >> 5);
+      const int64_t s1_end = static_cast<int64_t>(p.k128) * (((p.M + 31) >> 5) + 4 * p.G);
+      const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kComputeThreads + threadIdx.x;
+      const int64_t gstride = static_cast<int64_t>(gridDim.x) * kComputeThreads;
+      for (int64_t i = s0_beg / 4 + gtid; i < s0_end / 4; i += gstride)
+        reinterpret_cast<uint32_t*>(p.s0)[i] = 0u;
+      for (int64_t i = s1_beg / 4 + gtid; i < s1_end / 4; i += gstride)
+        reinterpret_cast<uint32_t*>(p.s1)[i] = 0u;
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_watchdog, 1);
+}
+
+}  // namespace
+
+// ---- host launchers -----------------------------------------------------------
+
+namespace {
+
+int set_smem(const void* fn) {
+  // Attribute set once per process and kernel; cheap to repeat but avoided.
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return e == cudaSuccess ? 0 : static_cast<int>(e);
+}
+
+template <int kMode>
+int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t stream) {
+  static int attr_rc = set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>));
+  if (attr_rc != 0) return attr_rc;
+  mx_cast_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(maps.x, maps.q0, maps.q1e, maps.q1o,
+                                                               prm);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+int smem_bytes_cast() { return kSmemBytes; }
+int threads_cast() { return kThreads; }
+
+int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, bool dim0, void* s0, void* s1,
+                   int num_sms, cudaStream_t stream) {
+  Params prm = {};
+  prm.M = M;
+  prm.K = K;
+  prm.n_mt = static_cast<int32_t>((M + kTile - 1) / kTile);
+  prm.n_kt = static_cast<int32_t>((K + kTile - 1) / kTile);
+  prm.n_tiles = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
+  prm.s0 = static_cast<uint8_t*>(s0);
+  prm.s1 = static_cast<uint8_t*>(s1);
+  const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
+  if (grid <= 0) return 0;
+  return dim0 ? launch<kModeFused2D>(maps, prm, grid, stream)
+              : launch<kModeDim1>(maps, prm, grid, stream);
+}
+
+int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* s1,
+                        int num_sms, cudaStream_t stream) {
+  Params prm = {};
+  prm.M = E * N;
+  prm.K = K;
+  prm.n_mt = static_cast<int32_t>((prm.M + kTile - 1) / kTile);
+  prm.n_kt = static_cast<int32_t>((K + kTile - 1) / kTile);
+  prm.n_tiles = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
+  prm.s1 = static_cast<uint8_t*>(s1);
+  prm.N = N;
+  prm.nb4 = static_cast<int32_t>(((N / 32) + 3) / 4 * 4);
+  prm.s1_expert_bytes = ((K + 127) / 128) * 128 * prm.nb4;
+  prm.s1_scatter = (N % 128) != 0;
+  const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
+  if (grid <= 0) return 0;
+  return launch<kModeExperts>(maps, prm, grid, stream);
+}
+
+int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_t* offs, int G,
+                        void* q1, void* s0, const int64_t* row_offs, void* s1,
+                        const int32_t* status, int num_sms, cudaStream_t stream) {
+  Params prm = {};
+  prm.M = M;
+  prm.K = K;
+  prm.n_kt = static_cast<int32_t>((K + kTile - 1) / kTile);
+  prm.n_mt = static_cast<int32_t>((M + kTile - 1) / kTile + G);   // upper bound
+  prm.s0 = static_cast<uint8_t*>(s0);
+  prm.s1 = static_cast<uint8_t*>(s1);
+  prm.q1 = static_cast<uint8_t*>(q1);
+  prm.offs = offs;
+  prm.row_offs = row_offs;
+  prm.status = status;
+  prm.G = G;
+  prm.k128 = static_cast<int32_t>((K + 127) / 128 * 128);
+  const int64_t bound = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
+  const int grid = static_cast<int>(bound < num_sms ? (bound > 0 ? bound : 1) : num_sms);
+  return launch<kModeGrouped>(maps, prm, grid, stream);
+}
+
+int read_watchdog(int* out, bool clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_watchdog, sizeof(int));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  if (clear && v) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_watchdog, &z, sizeof(int));
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
+  *out = v;
+  return 0;
+}
+
+}  // namespace mx

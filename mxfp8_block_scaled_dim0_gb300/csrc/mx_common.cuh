@@ -1,0 +1,208 @@
+// mx_common.cuh -- inline-PTX building blocks for the sm_103a MX-FP8 kernels:
+// mbarriers with bounded waits, TMA tile loads/stores, bulk copies, and the
+// per-block scale / element conversion of the MX rule.
+//
+// The rule (per 32-element block; OCP MX v1.0 conversion with E4M3 elements
+// and an E8M0 scale, blocks of 32 along either dimension as in pytorch/ao PR
+// #1869 "triton kernel to cast to mx across dim0 and dim1", summary):
+//   E     = biased exponent field of the block's largest |x| (bf16 bits)
+//   s     = max(E - 8, 0)          e8m0 byte; floor(log2 amax) - 8, clamped
+//   mult  = 2^(127 - s)            exact float built from bits
+//   q_i   = e4m3 of x_i * mult, round to nearest even, saturate to +-448
+// The exponent comes from integer bit fields (no float log, as the review of
+// that PR asks).  E == 255 (Inf or NaN in the block) gives s = 0xFF and NaN
+// elements.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace mx {
+
+// ---- shared-memory addressing ---------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarriers -------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Upper bound on any single wait.  Legitimate waits here last microseconds;
+// after this long the CTA gives up, raises its abort flag and winds down.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Wait for the phase of parity `parity` to complete.  Returns false if the
+// CTA-wide abort flag is (or becomes) set or the time limit passes; in the
+// latter case the flag is raised so that every other role stops too.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// ---- TMA (tensor) and bulk copies -------------------------------------------
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m, int32_t x,
+                                            int32_t y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t x, int32_t y,
+                                             const void* smem_src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::
+                   "l"(reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
+}
+
+// Plain bulk copy smem -> global; both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---- the MX rule -----------------------------------------------------------
+
+// Running |max| of packed bf16 pairs.  max.xorsign.abs takes the larger
+// magnitude of each half (with .NaN, a NaN wins); the sign bit it leaves is
+// meaningless and is masked off at the end.
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Magnitude bits (15 bits) of the low and high halves of an absmax2 result.
+__device__ __forceinline__ uint32_t mag_lo(uint32_t a) { return a & 0x7FFFu; }
+__device__ __forceinline__ uint32_t mag_hi(uint32_t a) { return (a >> 16) & 0x7FFFu; }
+
+// Scale byte and multiplier from a block's largest magnitude (bf16 bits).
+__device__ __forceinline__ void mx_scale(uint32_t amax_bits, uint32_t& sbyte, float& mult) {
+  const int E = static_cast<int>(amax_bits >> 7);           // 0..255
+  const int s = E > 8 ? E - 8 : 0;                           // 0..247
+  uint32_t mbits = static_cast<uint32_t>(254 - s) << 23;     // 2^(127 - s)
+  uint32_t b = static_cast<uint32_t>(s);
+  if (E == 255) {                                            // Inf / NaN block
+    b = 0xFFu;
+    mbits = 0x7FC00000u;                                     // NaN multiplier
+  }
+  sbyte = b;
+  mult = __uint_as_float(mbits);
+}
+
+// bf16 halves of a packed word as exact floats.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round-to-nearest product without flush-to-zero: subnormal bf16 inputs must
+// survive the multiply (a block of subnormals scales them up to e4m3 normals).
+__device__ __forceinline__ float mul_rn(float a, float b) {
+  float d;
+  asm("mul.rn.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Four floats (f0 at the lowest address) times mult -> four e4m3 bytes packed
+// little-endian.  cvt puts its first source in the high byte of each pair.
+__device__ __forceinline__ uint32_t e4m3x4(float f0, float f1, float f2, float f3, float m) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(mul_rn(f0, m)), "f"(mul_rn(f1, m)), "f"(mul_rn(f2, m)), "f"(mul_rn(f3, m)));
+  return r;
+}
+
+// Byte offset of scale (r, c) inside the 128x4 blocked tile that holds it:
+// 32 storage rows of 16 bytes; storage row r % 32 holds rows r, r+32, r+64,
+// r+96 (4 columns each).
+__device__ __forceinline__ int blocked_in_tile(int r, int c) {
+  return (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
+// Byte offset of scale (r, c) in the blocked layout of a matrix whose padded
+// column count is c4 (a multiple of 4): tiles of 128 x 4, row-major.
+__device__ __forceinline__ int64_t blocked_offset(int64_t r, int64_t c, int64_t c4) {
+  return ((r >> 7) * (c4 >> 2) + (c >> 2)) * 512 + blocked_in_tile(static_cast<int>(r & 127),
+                                                                    static_cast<int>(c & 3));
+}
+
+}  // namespace mx

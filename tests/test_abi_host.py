@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI library that need no GPU: it builds for
+sm_103a, loads, exports every function the header declares, computes sizes,
+and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mxfp8_block_scaled_dim0_gb300 as mx
+from mxfp8_block_scaled_dim0_gb300 import build as mxbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp8_cast.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mxbuild.build()
+    return mx.library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(mx_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    fns = header_functions()
+    assert set(fns) == set(mx.ABI_SYMBOLS), fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_size_helpers(lib):
+    assert mx.mx_blocked_bytes(1, 1) == 512
+    assert mx.mx_blocked_bytes(128, 4) == 512
+    assert mx.mx_blocked_bytes(129, 5) == 256 * 8
+    assert mx.mx_blocked_bytes(16384, 512) == 16384 * 512
+    assert mx.mx_blocked_bytes(-1, 4) == -1
+    # grouped bounds: rows + groups * 128 (dim0), columns ceil(M/32) + 4 G (dim1)
+    assert mx.mx_grouped_m_scale_bytes(16640, 5120, 4, 0) == (16640 + 512) * 160
+    assert mx.mx_grouped_m_scale_bytes(16640, 5120, 4, 1) == 5120 * (520 + 16)
+    assert mx.mx_grouped_m_scale_bytes(16640, 5120, 0, 0) == -1
+    assert mx.mx_3d_scale_bytes(16, 8192, 5120) == 16 * 5120 * 256
+    assert mx.mx_3d_scale_bytes(2, 96, 160) == 2 * 256 * 4
+
+
+def test_strerror(lib):
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert lib.mx_strerror(code)
+
+
+# Fake, never-dereferenced device addresses: argument checks run before any
+# CUDA call, so these return without touching a device.
+A = 1 << 20          # 16-byte aligned
+B = (1 << 20) + 8    # misaligned
+
+
+def test_cast_rejects_null(lib):
+    assert lib.mx_cast_dim0_dim1(None, 64, 64, A, A, A, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_dim0_dim1(A, 64, 64, A, None, A, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_dim1(A, 64, 64, None, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_scales_to_blocked(None, 4, 4, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_3d_dim1(A, 2, 64, 64, A, None, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_grouped_m(A, 64, 64, A, 2, A, A, A, A, A, A, None, None) == mx.MX_ERR_NULL
+
+
+@pytest.mark.parametrize("M,K", [(0, 64), (64, 0), (33, 64), (64, 48), (-32, 64), (1 << 31, 32)])
+def test_cast_rejects_shapes(lib, M, K):
+    assert lib.mx_cast_dim0_dim1(A, M, K, A, A, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_dim1(A, M, K, A, A, None) == mx.MX_ERR_SHAPE
+
+
+def test_other_shape_rules(lib):
+    assert lib.mx_scales_to_blocked(A, 0, 4, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_3d_dim1(A, 2, 48, 64, A, A, None) == mx.MX_ERR_SHAPE   # N % 32
+    assert lib.mx_cast_3d_dim1(A, 0, 64, 64, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_grouped_m(A, 64, 40, A, 2, A, A, A, A, A, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_grouped_m(A, 0, 64, A, 2, A, A, A, A, A, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_grouped_m(A, 64, 64, A, 0, A, A, A, A, A, A, A, None) == mx.MX_ERR_GROUPS
+
+
+def test_cast_rejects_misalignment(lib):
+    assert lib.mx_cast_dim0_dim1(B, 64, 64, A, A, A, A, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_dim0_dim1(A, 64, 64, A, A, B, A, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_dim1(A, 64, 64, A, B, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_scales_to_blocked(A, 4, 4, B, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_3d_dim1(A, 2, 64, 64, B, A, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_grouped_m(A, 64, 64, A + 2, 2, A, A, A, A, A, A, A, None) == mx.MX_ERR_ALIGN
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(mx, "_LIB", None)
+    monkeypatch.setattr(mx, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        mx.library()
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "mxfp8_block_scaled_dim0_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\b(import|from)\s+oracle\b|mx_oracle|oracle_\w+\(", text), f
