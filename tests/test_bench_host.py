@@ -1,0 +1,91 @@
+"""Host logic of bench.py on CPU: byte accounting, the whole-job value, the
+max-over-ranks timing with two gloo ranks, the clock-record parser, and the
+traffic file guard."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_algorithmic_bytes_match_the_buffers():
+    # 16384^2: 2 B read + 2 B written per element + two 8 MiB blocked buffers
+    assert bench.algorithmic_bytes(16384, 16384) == 4 * 16384 * 16384 + 2 * 16384 * 512
+    # ragged: padded blocked scale buffers are part of what must be written
+    assert bench.algorithmic_bytes(160, 96) == 4 * 160 * 96 + 256 * 4 + 128 * 8
+
+
+def test_whole_job_value():
+    assert bench.whole_job_value(1e9, 10, 2, 4.0) == pytest.approx(5.0)
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, ws, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    w, r, _ = bench.dist_env()
+    bench.barrier(w)
+    elapsed = 1.0 + rank            # rank 1 is the slow one
+    m = bench.max_over_ranks(elapsed, w)
+    out[rank] = (w, r, m, bench.whole_job_value(1e9, 4, w, m))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for r in range(2):
+        w, rr, m, v = out[r]
+        assert (w, rr) == (2, r)
+        assert m == 2.0                      # the slower rank's time, on every rank
+        assert v == pytest.approx(1e9 * 4 * 2 / 2.0 / 1e9)
+
+
+def test_clock_parser(tmp_path):
+    s = bench.ClockSampler(0)
+    s.path = str(tmp_path / "c.csv")
+    with open(s.path, "w") as f:
+        f.write("0, 1965 MHz, 2070 MHz, 700.00 W, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n")
+        f.write("0, 1980 MHz, 2070 MHz, 900.00 W, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n")
+        f.write("0, 1995 MHz, 2070 MHz, 910.00 W, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n")
+
+    class Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s.proc = Done()
+    info = s.stop()
+    assert info["sm_mhz"] == 1980.0 and info["sm_max_mhz"] == 2070.0
+    assert info["reasons"] == ["sw_power_cap"] and info["samples"] == 3
+
+
+def test_traffic_is_null_for_other_kernel_code(tmp_path, monkeypatch):
+    f = tmp_path / "t.txt"
+    f.write_text("kernel_source_sha256_16: 0000000000000000\ndram_bytes_per_full_launch: 123\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.measured_traffic() is None
+    f.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_full_launch: 123\n"
+                 % bench.kernel_source_hash())
+    assert bench.measured_traffic() == 123.0
