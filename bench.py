@@ -242,6 +242,10 @@ def run_gpu(args):
     mx.library()
 
     M, K = W.WORKLOADS[WORKLOAD].shape
+    workload = WORKLOAD
+    if args.shape:
+        M, K = args.shape
+        workload = "custom_%dx%d_weight" % (M, K)
     nbytes = algorithmic_bytes(M, K)
     stream = torch.cuda.current_stream(dev)
 
@@ -342,9 +346,9 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "shape": [M, K], "input": "bf16 N(0,1)*0.02",
+            "config": {"workload": workload, "shape": [M, K], "input": "bf16 N(0,1)*0.02",
                        "bytes_per_step": nbytes,
-                       "l2": "inputs 512 MiB > 129 MB L2; two buffer sets alternated",
+                       "l2": "inputs %d MiB > 129 MB L2; two buffer sets alternated" % (2 * M * K >> 20),
                        "parallelism": "replicas" if ws > 1 else "single"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
@@ -372,6 +376,8 @@ def main(argv=None):
     p.add_argument("--impl", choices=["mx", "reference"], default="mx")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--shape", type=int, nargs=2, metavar=("M", "K"), default=None,
+                   help="cast an M x K matrix of the same value mix instead (profiling)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
