@@ -64,20 +64,12 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
   return MX_OK;
 }
 
-// Descriptors for X (M x K bf16), q0 (M x K bytes) and q1 (K x M bytes, as
-// its even and odd rows).  q0 / q1 may be null (not used by the call).
-int encode_cast_maps(mx::CastMaps* maps, const void* x, int64_t M, int64_t K, const void* q0,
-                     const void* q1) {
+// Descriptors for X (M x K bf16) and q1 (K x M bytes, as its even and odd
+// rows).  q1 may be null (not written by TMA in this call).
+int encode_cast_maps(mx::CastMaps* maps, const void* x, int64_t M, int64_t K, const void* q1) {
   int rc = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, 128,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
-  if (q0) {
-    rc = encode_2d(&maps->q0, CU_TENSOR_MAP_DATA_TYPE_UINT8, q0, K, M, K, 128, 128,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
-    if (rc) return rc;
-  } else {
-    maps->q0 = maps->x;   // never dereferenced
-  }
   if (q1) {
     rc = encode_2d(&maps->q1e, CU_TENSOR_MAP_DATA_TYPE_UINT8, q1, M, K / 2, 2 * M, 128, 64,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
@@ -158,10 +150,10 @@ int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_bl
       !aligned(s1_blk, 16))
     return MX_ERR_ALIGN;
   mx::CastMaps maps;
-  if (int rc = encode_cast_maps(&maps, x, M, K, q0, q1)) return rc;
+  if (int rc = encode_cast_maps(&maps, x, M, K, q1)) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
-  return launch_rc(mx::launch_cast_2d(maps, M, K, true, s0_blk, s1_blk, sms,
+  return launch_rc(mx::launch_cast_2d(maps, M, K, q0, s0_blk, s1_blk, sms,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -170,10 +162,10 @@ int mx_cast_dim1(const void* x, int64_t M, int64_t K, void* q1, void* s1_blk, vo
   if (int rc = check_2d_shape(M, K)) return rc;
   if (!aligned(x, 16) || !aligned(q1, 16) || !aligned(s1_blk, 16)) return MX_ERR_ALIGN;
   mx::CastMaps maps;
-  if (int rc = encode_cast_maps(&maps, x, M, K, nullptr, q1)) return rc;
+  if (int rc = encode_cast_maps(&maps, x, M, K, q1)) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
-  return launch_rc(mx::launch_cast_2d(maps, M, K, false, nullptr, s1_blk, sms,
+  return launch_rc(mx::launch_cast_2d(maps, M, K, nullptr, nullptr, s1_blk, sms,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -200,14 +192,14 @@ int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, 
     return MX_ERR_ALIGN;
   mx::CastMaps maps;
   // q1 is written with plain stores (group starts are not 16-byte aligned).
-  if (int rc = encode_cast_maps(&maps, x, M, K, q0, nullptr)) return rc;
+  if (int rc = encode_cast_maps(&maps, x, M, K, nullptr)) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (int rc = mx::launch_group_offsets(offs, G, M, s0_row_offs, s1_col_offs, status, st))
     return cuda_fail(rc);
-  return launch_rc(mx::launch_cast_grouped(maps, M, K, offs, G, q1, s0_blk, s0_row_offs, s1_blk,
-                                           status, sms, st));
+  return launch_rc(mx::launch_cast_grouped(maps, M, K, offs, G, q0, q1, s0_blk, s0_row_offs,
+                                           s1_blk, status, sms, st));
 }
 
 int mx_cast_3d_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q1, void* s1_blk,
@@ -218,7 +210,7 @@ int mx_cast_3d_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q1, vo
   if (!aligned(w, 16) || !aligned(q1, 16) || !aligned(s1_blk, 16)) return MX_ERR_ALIGN;
   const int64_t M = E * N;
   mx::CastMaps maps;
-  if (int rc = encode_cast_maps(&maps, w, M, K, nullptr, q1)) return rc;
+  if (int rc = encode_cast_maps(&maps, w, M, K, q1)) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -17,12 +17,18 @@
 // 128x4 blocked scale tile per direction, so the swizzle costs nothing.
 //
 // CTA roles (one CTA per SM, persistent over tiles):
-//   warps 0-7  compute: dim0 and dim1 block maxima, scales, e4m3 packing,
-//              into swizzled shared-memory staging tiles
+//   warps 0-7  compute: dim0 and dim1 block maxima, scales, e4m3 packing.
+//              dim0 bytes go straight to global memory (each warp store
+//              writes four whole 128-byte rows of q0); dim1 bytes go to a
+//              swizzled shared-memory staging tile
 //   warp 8     producer: TMA loads of the bf16 tile (two 64-column halves,
 //              128B swizzle) into a kStages-deep ring
-//   warp 9     storer: TMA stores of the staged fp8 tiles and bulk copies of
-//              the 512-byte scale tiles
+//   warp 9     storer: TMA stores of the staged q1 tile, bulk copy of the
+//              dim0 scale tile, and the dim1 scale tile (staged in plain
+//              order, transposed to the blocked order on the way out)
+// The depths were chosen by measurement on GB300: few input stages and many
+// output staging buffers.  More loads in flight (4-5 stages) slowed the
+// kernel by ~12%: outstanding writes, not reads, limit the mixed stream.
 // Every wait is bounded (see mbar_wait); on time-out the CTA raises an abort
 // flag, stops, drains its own bulk copies and reports through a device word.
 #include <cuda_runtime.h>
@@ -43,7 +49,8 @@ constexpr int kInBytes = 2 * kHalfBytes;    // one bf16 tile
 constexpr int kQBytes = 128 * 128;          // one e4m3 tile
 constexpr int kQ1Half = 64 * 128;           // even / odd columns of a q1 tile
 constexpr int kScaleTile = 512;
-constexpr int kStages = 4;
+constexpr int kStages = 3;                 // input ring depth
+constexpr int kStaging = 6;                // q1 / scale staging buffers
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kThreads = kComputeThreads + 64;
@@ -53,12 +60,11 @@ constexpr int kStoreWarp = kComputeWarps + 1;
 // Shared-memory layout, offsets from a 1024-byte aligned base (the 128B
 // swizzle pattern repeats every 1024 bytes).
 constexpr int kOffIn = 0;
-constexpr int kOffQ0 = kOffIn + kStages * kInBytes;
-constexpr int kOffQ1 = kOffQ0 + 2 * kQBytes;
-constexpr int kOffS0 = kOffQ1 + 2 * kQBytes;
-constexpr int kOffS1 = kOffS0 + 2 * kScaleTile;
-constexpr int kOffBar = kOffS1 + 2 * kScaleTile;
-constexpr int kNumBars = 2 * kStages + 6;
+constexpr int kOffQ1 = kOffIn + kStages * kInBytes;
+constexpr int kOffS0 = kOffQ1 + kStaging * kQBytes;
+constexpr int kOffS1 = kOffS0 + kStaging * kScaleTile;
+constexpr int kOffBar = kOffS1 + kStaging * kScaleTile;
+constexpr int kNumBars = 2 * kStages + 3 * kStaging;
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -82,6 +88,7 @@ struct Params {
   int64_t n_tiles;          // 2D / 3D modes
   uint8_t* s0;
   uint8_t* s1;
+  uint8_t* q0;              // dim0 data, written directly
   uint8_t* q1;              // grouped mode: plain stores of q1
   // experts (3D)
   int64_t N;                // rows per expert
@@ -149,43 +156,43 @@ __device__ __forceinline__ Tile get_tile(const Params& p, int64_t t) {
 
 // ---- compute units ----------------------------------------------------------
 
-// dim0 unit: one 32-element block (row `row`, block `b` of 4) of the tile.
-// Reads four 16-byte chunks of the 128B-swizzled input, writes 32 e4m3 bytes
-// to the swizzled q0 staging tile and one scale byte to the staging scale
-// tile.  Rows at or beyond `rows` get scale 0 (padding of a group).
-__device__ __forceinline__ void dim0_unit(const uint8_t* in, uint8_t* q0s, uint8_t* sc0,
-                                          int row, int b, int rows) {
+// dim0 half-block unit (16 elements), stored straight to q0.  In warp step
+// with first row R0 (even), lane l takes row R0 + ((l >> 2) & 1) + 2*(l >> 4),
+// 64-column half `box` = (l >> 3) & 1 and half-block hq = l & 3 of that half:
+//   - each 8-lane phase of a 16-byte shared load touches two rows of one half
+//     whose swizzles differ in the lowest bit, so all 8 bank groups differ;
+//   - each warp store writes four whole 128-byte rows of q0;
+//   - lanes l and l^1 hold the two halves of one 32-element block and combine
+//     their maxima with one shuffle.
+// Rows at or beyond `rows` (grouped mode: past the group's end) are neither
+// stored nor given a scale (their blocked scale byte is padding, 0).
+__device__ __forceinline__ void dim0_half_unit(const uint8_t* in, uint8_t* sc0, uint8_t* q0,
+                                               int64_t M, int64_t K, int m0, int k0, int R0,
+                                               int lane, int rows) {
+  const int row = R0 + ((lane >> 2) & 1) + 2 * (lane >> 4);
+  const int box = (lane >> 3) & 1;
+  const int hq = lane & 3;
   const int sw = row & 7;
-  const uint8_t* src = in + (b >> 1) * kHalfBytes + row * 128;
-  uint4 v[4];
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    const int q = ((b & 1) << 2) + h;
-    v[h] = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
-  }
-  uint32_t a0 = absmax2(absmax2(v[0].x, v[0].y), absmax2(v[0].z, v[0].w));
-  uint32_t a1 = absmax2(absmax2(v[1].x, v[1].y), absmax2(v[1].z, v[1].w));
-  uint32_t a2 = absmax2(absmax2(v[2].x, v[2].y), absmax2(v[2].z, v[2].w));
-  uint32_t a3 = absmax2(absmax2(v[3].x, v[3].y), absmax2(v[3].z, v[3].w));
-  const uint32_t a = absmax2(absmax2(a0, a1), absmax2(a2, a3));
+  const uint8_t* src = in + box * kHalfBytes + row * 128;
+  const uint4 v0 = *reinterpret_cast<const uint4*>(src + (((2 * hq) ^ sw) << 4));
+  const uint4 v1 = *reinterpret_cast<const uint4*>(src + (((2 * hq + 1) ^ sw) << 4));
+  uint32_t a = absmax2(absmax2(absmax2(v0.x, v0.y), absmax2(v0.z, v0.w)),
+                       absmax2(absmax2(v1.x, v1.y), absmax2(v1.z, v1.w)));
+  a = absmax2(a, __shfl_xor_sync(0xffffffffu, a, 1));
   const uint32_t lo = mag_lo(a), hi = mag_hi(a);
   uint32_t sbyte;
   float m;
   mx_scale(lo > hi ? lo : hi, sbyte, m);
-
-  uint4 o0, o1;
-  o0.x = e4m3x4(bf_lo(v[0].x), bf_hi(v[0].x), bf_lo(v[0].y), bf_hi(v[0].y), m);
-  o0.y = e4m3x4(bf_lo(v[0].z), bf_hi(v[0].z), bf_lo(v[0].w), bf_hi(v[0].w), m);
-  o0.z = e4m3x4(bf_lo(v[1].x), bf_hi(v[1].x), bf_lo(v[1].y), bf_hi(v[1].y), m);
-  o0.w = e4m3x4(bf_lo(v[1].z), bf_hi(v[1].z), bf_lo(v[1].w), bf_hi(v[1].w), m);
-  o1.x = e4m3x4(bf_lo(v[2].x), bf_hi(v[2].x), bf_lo(v[2].y), bf_hi(v[2].y), m);
-  o1.y = e4m3x4(bf_lo(v[2].z), bf_hi(v[2].z), bf_lo(v[2].w), bf_hi(v[2].w), m);
-  o1.z = e4m3x4(bf_lo(v[3].x), bf_hi(v[3].x), bf_lo(v[3].y), bf_hi(v[3].y), m);
-  o1.w = e4m3x4(bf_lo(v[3].z), bf_hi(v[3].z), bf_lo(v[3].w), bf_hi(v[3].w), m);
-  uint8_t* dst = q0s + row * 128;
-  *reinterpret_cast<uint4*>(dst + (((2 * b) ^ sw) << 4)) = o0;
-  *reinterpret_cast<uint4*>(dst + (((2 * b + 1) ^ sw) << 4)) = o1;
-  sc0[blocked_in_tile(row, b)] = static_cast<uint8_t>(row < rows ? sbyte : 0u);
+  uint4 o;
+  o.x = e4m3x4(bf_lo(v0.x), bf_hi(v0.x), bf_lo(v0.y), bf_hi(v0.y), m);
+  o.y = e4m3x4(bf_lo(v0.z), bf_hi(v0.z), bf_lo(v0.w), bf_hi(v0.w), m);
+  o.z = e4m3x4(bf_lo(v1.x), bf_hi(v1.x), bf_lo(v1.y), bf_hi(v1.y), m);
+  o.w = e4m3x4(bf_lo(v1.z), bf_hi(v1.z), bf_lo(v1.w), bf_hi(v1.w), m);
+  const int64_t gr = static_cast<int64_t>(m0) + row;
+  const int64_t gc = static_cast<int64_t>(k0) + 64 * box + 16 * hq;
+  if (row < rows && gr < M && gc < K) *reinterpret_cast<uint4*>(q0 + gr * K + gc) = o;
+  if ((hq & 1) == 0)
+    sc0[blocked_in_tile(row, 2 * box + (hq >> 1))] = static_cast<uint8_t>(row < rows ? sbyte : 0u);
 }
 
 // Four consecutive rows of one column of a dim1 unit -> four e4m3 bytes.
@@ -196,7 +203,9 @@ __device__ __forceinline__ void dim0_unit(const uint8_t* in, uint8_t* q0s, uint8
 // 32*mb+31.  Reads one 4-byte word per row (a warp reads whole 128-byte rows,
 // conflict-free under the swizzle), writes 32 e4m3 bytes per column into the
 // even / odd halves of the q1 staging tile (row p of each half) and the two
-// scale bytes.  Rows at or beyond `rows` are treated as zero (grouped mode).
+// scale bytes, as one 16-bit store into the plain-order scale staging
+// [mb][column] (conflict-free; the store warp transposes it to the blocked
+// order).  Rows at or beyond `rows` are treated as zero (grouped mode).
 // Returns the two scale bytes (even column in bits 0-7, odd in 8-15).
 template <bool kMask>
 __device__ __forceinline__ uint32_t dim1_unit(const uint8_t* in, uint8_t* q1s, uint8_t* sc1,
@@ -242,9 +251,9 @@ __device__ __forceinline__ uint32_t dim1_unit(const uint8_t* in, uint8_t* q1s, u
   *reinterpret_cast<uint4*>(de + (((2 * mb + 1) ^ sw) << 4)) = e1;
   *reinterpret_cast<uint4*>(dodd + (((2 * mb) ^ sw) << 4)) = o0;
   *reinterpret_cast<uint4*>(dodd + (((2 * mb + 1) ^ sw) << 4)) = o1;
-  sc1[blocked_in_tile(2 * p, mb)] = static_cast<uint8_t>(se);
-  sc1[blocked_in_tile(2 * p + 1, mb)] = static_cast<uint8_t>(so);
-  return se | (so << 8);
+  const uint32_t pair = se | (so << 8);
+  *reinterpret_cast<uint16_t*>(sc1 + mb * 128 + 2 * p) = static_cast<uint16_t>(pair);
+  return pair;
 }
 #undef MX_COL4_LO
 #undef MX_COL4_HI
@@ -290,19 +299,19 @@ __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* q1, int
 
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    mx_cast_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q0,
-                   const __grid_constant__ CUtensorMap tm_q1e,
+    mx_cast_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q1e,
                    const __grid_constant__ CUtensorMap tm_q1o, const Params p) {
   constexpr bool kDim0 = (kMode == kModeFused2D || kMode == kModeGrouped);
+  constexpr bool kTmaQ1 = (kMode != kModeGrouped);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bars;                  // [kStages] TMA landed
-  uint64_t* empty = bars + kStages;       // [kStages] compute done reading
-  uint64_t* sfull = bars + 2 * kStages;   // [2] staging written
-  uint64_t* sempty = sfull + 2;           // [2] staging read by the bulk engine
-  uint64_t* qstaged = sfull + 4;          // [2] grouped: q1 staging complete
+  uint64_t* full = bars;                      // [kStages] TMA landed
+  uint64_t* empty = bars + kStages;           // [kStages] compute done reading
+  uint64_t* sfull = bars + 2 * kStages;       // [kStaging] staging written
+  uint64_t* sempty = sfull + kStaging;        // [kStaging] staging drained
+  uint64_t* qstaged = sfull + 2 * kStaging;   // [kStaging] grouped: q1 staged
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
 
   const int warp = threadIdx.x >> 5;
@@ -310,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int64_t n_tiles;
   if (kMode == kModeGrouped) {
-    if (*p.status != 0) return;           // invalid group offsets: write nothing
+    if (*p.status != 0) return;               // invalid group offsets: write nothing
     n_tiles = grouped_tiles(p);
   } else {
     n_tiles = p.n_tiles;
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kComputeWarps);
     }
-    for (int o = 0; o < 2; ++o) {
+    for (int o = 0; o < kStaging; ++o) {
       mbar_init(&sfull[o], kComputeWarps);
       mbar_init(&sempty[o], 1);
       mbar_init(&qstaged[o], kComputeWarps);
@@ -351,33 +360,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kStoreWarp) {
-    if (lane == 0) {
-      if (kDim0) prefetch_tmap(&tm_q0);
-      if (kMode != kModeGrouped) {
-        prefetch_tmap(&tm_q1e);
-        prefetch_tmap(&tm_q1o);
-      }
-      int64_t it = 0;
-      for (int64_t t = first; t < n_tiles; t += step, ++it) {
-        const int o = static_cast<int>(it & 1);
-        const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
-        if (!mbar_wait(&sfull[o], ph, abort_flag)) break;
-        const Tile T = get_tile<kMode>(p, t);
-        if (kDim0) {
-          tma_store_2d(&tm_q0, T.k0, T.m0, smem + kOffQ0 + o * kQBytes);
-          bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
-        }
-        if (kMode != kModeGrouped) {
+    if (lane == 0 && kTmaQ1) {
+      prefetch_tmap(&tm_q1e);
+      prefetch_tmap(&tm_q1o);
+    }
+    int64_t it = 0;
+    for (int64_t t = first; t < n_tiles; t += step, ++it) {
+      const int o = static_cast<int>(it % kStaging);
+      const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
+      const bool ok = mbar_wait(&sfull[o], ph, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const Tile T = get_tile<kMode>(p, t);
+      if (lane == 0) {
+        if (kTmaQ1) {
           tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes);
           tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes + kQ1Half);
         }
-        if (T.s1_dst) bulk_store(T.s1_dst, smem + kOffS1 + o * kScaleTile, kScaleTile);
+        if (kDim0) bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
         bulk_commit();
+      }
+      if (T.s1_dst) {
+        // dim1 scales are staged as [M-block][column]; storage row `lane` of
+        // the blocked tile holds columns lane, lane+32, lane+64, lane+96, four
+        // M-blocks each.
+        const uint8_t* nat = smem + kOffS1 + o * kScaleTile;
+        uint4 w;
+        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int c = lane + 32 * a;
+          wp[a] = static_cast<uint32_t>(nat[c]) | (static_cast<uint32_t>(nat[128 + c]) << 8) |
+                  (static_cast<uint32_t>(nat[256 + c]) << 16) |
+                  (static_cast<uint32_t>(nat[384 + c]) << 24);
+        }
+        *reinterpret_cast<uint4*>(T.s1_dst + lane * 16) = w;
+      }
+      __syncwarp();
+      if (lane == 0) {
         bulk_wait_read<0>();
         mbar_arrive(&sempty[o]);
       }
-      bulk_wait<0>();
     }
+    if (lane == 0) bulk_wait<0>();
     __syncwarp();
   } else {
     // compute warps
@@ -385,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = first; t < n_tiles; t += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
-      const int o = static_cast<int>(it & 1);
-      const uint32_t oph = static_cast<uint32_t>((it >> 1) & 1);
+      const int o = static_cast<int>(it % kStaging);
+      const uint32_t oph = static_cast<uint32_t>((it / kStaging) & 1);
       bool ok = mbar_wait(&full[s], ph, abort_flag);
       ok = ok && mbar_wait(&sempty[o], oph ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -396,13 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
       uint8_t* sc1 = smem + kOffS1 + o * kScaleTile;
       if (kDim0) {
-        uint8_t* q0s = smem + kOffQ0 + o * kQBytes;
         uint8_t* sc0 = smem + kOffS0 + o * kScaleTile;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int row = (2 * warp + u) * 8 + (lane & 7);
-          dim0_unit(in, q0s, sc0, row, lane >> 3, T.rows);
-        }
+        for (int u = 0; u < 4; ++u)
+          dim0_half_unit(in, sc0, p.q0, p.M, p.K, T.m0, T.k0, (4 * warp + u) * 4, lane, T.rows);
       }
       const int mb = warp >> 1;
       const int pcol = (warp & 1) * 32 + lane;
@@ -482,8 +503,7 @@ template <int kMode>
 int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t stream) {
   static int attr_rc = set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>));
   if (attr_rc != 0) return attr_rc;
-  mx_cast_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(maps.x, maps.q0, maps.q1e, maps.q1o,
-                                                               prm);
+  mx_cast_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(maps.x, maps.q1e, maps.q1o, prm);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -492,9 +512,11 @@ int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t strea
 int smem_bytes_cast() { return kSmemBytes; }
 int threads_cast() { return kThreads; }
 
-int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, bool dim0, void* s0, void* s1,
+int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0, void* s1,
                    int num_sms, cudaStream_t stream) {
+  const bool dim0 = q0 != nullptr;
   Params prm = {};
+  prm.q0 = static_cast<uint8_t*>(q0);
   prm.M = M;
   prm.K = K;
   prm.n_mt = static_cast<int32_t>((M + kTile - 1) / kTile);
@@ -527,9 +549,10 @@ int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, v
 }
 
 int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_t* offs, int G,
-                        void* q1, void* s0, const int64_t* row_offs, void* s1,
+                        void* q0, void* q1, void* s0, const int64_t* row_offs, void* s1,
                         const int32_t* status, int num_sms, cudaStream_t stream) {
   Params prm = {};
+  prm.q0 = static_cast<uint8_t*>(q0);
   prm.M = M;
   prm.K = K;
   prm.n_kt = static_cast<int32_t>((K + kTile - 1) / kTile);

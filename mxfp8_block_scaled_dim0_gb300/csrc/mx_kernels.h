@@ -9,10 +9,9 @@
 namespace mx {
 
 // TMA descriptors of one cast call: x (bf16, two 64-column halves per tile,
-// 128B swizzle), q0 (e4m3 tile 128 x 128), q1 even / odd rows (64 x 128).
+// 128B swizzle) and the even / odd rows of q1 (64 x 128-byte boxes).
 struct CastMaps {
   CUtensorMap x;
-  CUtensorMap q0;
   CUtensorMap q1e;
   CUtensorMap q1o;
 };
@@ -21,12 +20,13 @@ int smem_bytes_cast();
 int threads_cast();
 
 // All launchers return 0 or a cudaError_t value.
-int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, bool dim0, void* s0, void* s1,
+// q0 == nullptr: dim1 only.
+int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0, void* s1,
                    int num_sms, cudaStream_t stream);
 int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* s1,
                         int num_sms, cudaStream_t stream);
 int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_t* offs, int G,
-                        void* q1, void* s0, const int64_t* row_offs, void* s1,
+                        void* q0, void* q1, void* s0, const int64_t* row_offs, void* s1,
                         const int32_t* status, int num_sms, cudaStream_t stream);
 int launch_group_offsets(const int32_t* offs, int G, int64_t M, int64_t* row_offs,
                          int64_t* col_offs, int32_t* status, cudaStream_t stream);
