@@ -8,6 +8,11 @@ written per element, plus the padded blocked scales) per second of device
 time, and its fraction of the measured GB300 copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mx|reference]
+                  [--row fused|dim1|grouped|experts|blocked] [--workload NAME]
+
+--row times another row of the hot path instead (one JSON line each): the
+dim1-only cast, the grouped-M MoE cast (16640 x 5120, 4 groups), the 3D expert
+dim1 cast (16 x 8192 x 5120) or the standalone scale blocking (262144 x 512).
 
 --impl reference times the CPU oracle (the plain C implementation used by the
 tests) on the host cores on a bounded sample of the same workload.  Under
@@ -227,6 +232,98 @@ def run_reference(args, budget_s=90.0):
 
 # ---- GPU arm ----------------------------------------------------------------------
 
+def blk(R, C):
+    return -(-R // 128) * 128 * (-(-C // 4) * 4)
+
+
+class Row:
+    """One scope row of the hot path as a timed step: how to build its buffers,
+    how to call it through the binding, and the bytes it must move."""
+
+    def __init__(self, name, workload, kernel, bytes_per_step, launches, build, call,
+                 inputs, outputs):
+        self.name, self.workload, self.kernel = name, workload, kernel
+        self.bytes_per_step, self.launches = bytes_per_step, launches
+        self.build, self.call, self.inputs, self.outputs = build, call, inputs, outputs
+
+
+def make_row(row, args, dev, rank):
+    import torch
+    import mxfp8_block_scaled_dim0_gb300 as mx
+    from mxfp8_block_scaled_dim0_gb300 import workloads as W
+    u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+
+    if row in ("fused", "dim1"):
+        wl = args.workload or WORKLOAD
+        if args.shape:
+            M, K = args.shape
+            wl = "custom_%dx%d_weight" % (M, K)
+            gen = lambda i: W.normal((M, K), 1003 + 100 * i + rank, device=dev, std=0.02)
+        else:
+            M, K = W.WORKLOADS[wl].shape
+            gen = lambda i: W.make(wl, device=dev)["x"] if i == 0 else \
+                W.normal((M, K), W.WORKLOADS[wl].seed + 100 * i + rank, device=dev, std=0.02)
+        if row == "fused":
+            def build(i):
+                return (gen(i), torch.empty((M, K), dtype=torch.uint8, device=dev),
+                        u8(mx.mx_blocked_bytes(M, K // 32)),
+                        torch.empty((K, M), dtype=torch.uint8, device=dev),
+                        u8(mx.mx_blocked_bytes(K, M // 32)))
+            return Row("fused", wl, "mx_cast_kernel<fused2d>", algorithmic_bytes(M, K), 1, build,
+                       lambda a, st: mx.mx_cast_dim0_dim1(*a, stream=st), (0,), (1, 2, 3, 4))
+
+        def build(i):
+            return (gen(i), torch.empty((K, M), dtype=torch.uint8, device=dev),
+                    u8(mx.mx_blocked_bytes(K, M // 32)))
+        return Row("dim1", wl, "mx_cast_kernel<dim1>", 2 * M * K + M * K + blk(K, M // 32), 1,
+                   build, lambda a, st: mx.mx_cast_dim1(*a, stream=st), (0,), (1, 2))
+
+    if row == "grouped":
+        wl = args.workload or "moe16640x5120_g4"
+        M, K = W.WORKLOADS[wl].shape
+        G = W.WORKLOADS[wl].groups
+        n0 = mx.mx_grouped_m_scale_bytes(M, K, G, 0)
+        n1 = mx.mx_grouped_m_scale_bytes(M, K, G, 1)
+
+        def build(i):
+            w = W.make(wl, device=dev)
+            x = w["x"] if i == 0 else W.normal((M, K), W.WORKLOADS[wl].seed + 100 * i, device=dev)
+            return (x, w["offs"].to(dev), torch.empty((M, K), dtype=torch.uint8, device=dev), u8(n0),
+                    torch.empty(G + 1, dtype=torch.int64, device=dev),
+                    torch.empty((K, M), dtype=torch.uint8, device=dev), u8(n1),
+                    torch.empty(G + 1, dtype=torch.int64, device=dev),
+                    torch.empty(1, dtype=torch.int32, device=dev))
+        nbytes = 2 * M * K + 4 * G + M * K + n0 + M * K + n1 + 16 * (G + 1) + 4
+        return Row("grouped", wl, "group_offsets_kernel + mx_cast_kernel<grouped>", nbytes, 2,
+                   build, lambda a, st: mx.mx_cast_grouped_m(*a, stream=st), (0, 1),
+                   (2, 3, 4, 5, 6, 7, 8))
+
+    if row == "experts":
+        wl = args.workload or "experts16x8192x5120"
+        E, N, K = W.WORKLOADS[wl].shape
+        ns = mx.mx_3d_scale_bytes(E, N, K)
+
+        def build(i):
+            w = W.make(wl, device=dev)["x"] if i == 0 else \
+                W.experts(E, N, K, W.WORKLOADS[wl].seed + 100 * i, device=dev)
+            return (w, torch.empty((K, E * N), dtype=torch.uint8, device=dev), u8(ns))
+        return Row("experts", wl, "mx_cast_kernel<experts>", 3 * E * N * K + ns, 1, build,
+                   lambda a, st: mx.mx_cast_3d_dim1(*a, stream=st), (0,), (1, 2))
+
+    if row == "blocked":
+        R, C = args.shape or (262144, 512)
+        wl = "scales_%dx%d" % (R, C)
+
+        def build(i):
+            g = torch.Generator(device=dev)
+            g.manual_seed(77 + i)
+            s = torch.randint(0, 256, (R, C), dtype=torch.uint8, device=dev, generator=g)
+            return (s, u8(mx.mx_blocked_bytes(R, C)))
+        return Row("blocked", wl, "to_blocked_kernel", R * C + blk(R, C), 1, build,
+                   lambda a, st: mx.mx_scales_to_blocked(*a, stream=st), (0,), (1,))
+    raise ValueError(row)
+
+
 def run_gpu(args):
     import torch
     ws, rank, local = dist_env()
@@ -238,50 +335,43 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
 
     import mxfp8_block_scaled_dim0_gb300 as mx
-    from mxfp8_block_scaled_dim0_gb300 import workloads as W
     mx.library()
 
-    M, K = W.WORKLOADS[WORKLOAD].shape
-    workload = WORKLOAD
-    if args.shape:
-        M, K = args.shape
-        workload = "custom_%dx%d_weight" % (M, K)
-    nbytes = algorithmic_bytes(M, K)
+    R = make_row(args.row, args, dev, rank)
+    nbytes = R.bytes_per_step
     stream = torch.cuda.current_stream(dev)
-
-    # Two input / output sets (each well above the 129 MB L2), alternated.
-    sets = []
-    for i in range(2):
-        x = W.normal((M, K), W.WORKLOADS[WORKLOAD].seed + 100 * i + rank, device=dev, std=0.02)
-        q0 = torch.empty((M, K), dtype=torch.uint8, device=dev)
-        q1 = torch.empty((K, M), dtype=torch.uint8, device=dev)
-        s0 = torch.empty(mx.mx_blocked_bytes(M, K // 32), dtype=torch.uint8, device=dev)
-        s1 = torch.empty(mx.mx_blocked_bytes(K, M // 32), dtype=torch.uint8, device=dev)
-        sets.append((x, q0, s0, q1, s1))
+    # Two buffer sets, each larger than the 129 MB L2, alternated step by step.
+    sets = [R.build(0), R.build(1)]
 
     def step(i):
-        x, q0, s0, q1, s1 = sets[i & 1]
-        mx.mx_cast_dim0_dim1(x, q0, s0, q1, s1, stream)
+        R.call(sets[i & 1], stream)
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
 
-    # timed region: K steps, an event pair around each launch and around all
+    # Timed region: K steps between two events; every 8th step also gets its
+    # own event pair, for the per-launch duration of the kernel.
+    every = 8
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(0, args.steps, every)]
     t_beg = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev.index if ws > 1 else int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0))
+    gpu_index = dev.index if ws > 1 else int(
+        (os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0").strip() or 0)
+    clocks = ClockSampler(gpu_index)
     barrier(ws)
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.15)
     t_beg.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(i)
-        ev[i][1].record(stream)
+        if i % every == 0:
+            ev[i // every][0].record(stream)
+            step(i)
+            ev[i // every][1].record(stream)
+        else:
+            step(i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clock_info = clocks.stop()
@@ -294,26 +384,21 @@ def run_gpu(args):
     peak, peak_kind = hbm_peak()
     achieved = nbytes / avg_launch / 1e9
 
-    # end-to-end through the public API with host buffers: pinned H2D of the
-    # input, the cast, D2H of all four outputs, every step
+    # End to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the call, D2H of every output, each step.
     e2e = None
     if args.e2e_steps > 0:
-        x, q0, s0, q1, s1 = sets[0]
-        hx = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
-        hx.copy_(x)
-        hq0 = torch.empty_like(q0, device="cpu").pin_memory()
-        hq1 = torch.empty_like(q1, device="cpu").pin_memory()
-        hs0 = torch.empty_like(s0, device="cpu").pin_memory()
-        hs1 = torch.empty_like(s1, device="cpu").pin_memory()
-        dx = sets[1][0]
+        dev_set = sets[0]
+        host_in = {j: dev_set[j].cpu().pin_memory() for j in R.inputs}
+        host_out = {j: torch.empty(dev_set[j].shape, dtype=dev_set[j].dtype).pin_memory()
+                    for j in R.outputs}
 
         def e2e_step():
-            dx.copy_(hx, non_blocking=True)
-            mx.mx_cast_dim0_dim1(dx, q0, s0, q1, s1, stream)
-            hq0.copy_(q0, non_blocking=True)
-            hs0.copy_(s0, non_blocking=True)
-            hq1.copy_(q1, non_blocking=True)
-            hs1.copy_(s1, non_blocking=True)
+            for j in R.inputs:
+                dev_set[j].copy_(host_in[j], non_blocking=True)
+            R.call(dev_set, stream)
+            for j in R.outputs:
+                host_out[j].copy_(dev_set[j], non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -326,39 +411,45 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize(dev)
         e_el = max_over_ranks(a.elapsed_time(b) / 1e3, ws, dev)
-        h2d = 2 * M * K
-        d2h = q0.numel() + q1.numel() + s0.numel() + s1.numel()
+        h2d = sum(host_in[j].numel() * host_in[j].element_size() for j in R.inputs)
+        d2h = sum(host_out[j].numel() * host_out[j].element_size() for j in R.outputs)
         e2e = {"value": whole_job_value(nbytes, args.e2e_steps, ws, e_el), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps, "ms_per_step": 1e3 * e_el / args.e2e_steps}
-        del hx, hq0, hq1, hs0, hs1
+        del host_in, host_out
 
     cpu = None
-    if rank == 0 and ws == 1 and args.cpu_seconds > 0:
+    if rank == 0 and ws == 1 and args.cpu_seconds > 0 and R.name == "fused" and not args.shape:
         gbs, rows, secs = time_oracle(seconds_budget=args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "first %d rows x %d cols of the workload (same value mix), %.1f s, "
-                         "fused dim0+dim1+blocked scales, single thread" % (rows, K, secs)}
+               "sample": "first %d rows x 16384 cols of the 16384x16384 workload (same value "
+                         "mix), %.1f s, fused dim0+dim1+blocked scales, single thread"
+                         % (rows, secs)}
 
     if rank == 0:
+        shape = list(sets[0][0].shape)
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "metric": METRIC if R.name == "fused" else METRIC.replace("fused MXFP8 dim0+dim1 cast",
+                                                                      "MXFP8 %s" % R.name),
+            "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": workload, "shape": [M, K], "input": "bf16 N(0,1)*0.02",
+            "config": {"workload": R.workload, "row": R.name, "shape": shape,
                        "bytes_per_step": nbytes,
-                       "l2": "inputs %d MiB > 129 MB L2; two buffer sets alternated" % (2 * M * K >> 20),
+                       "l2": "inputs %d MiB each, two buffer sets alternated (L2 is 129 MB)"
+                             % (sets[0][0].numel() * sets[0][0].element_size() >> 20),
                        "parallelism": "replicas" if ws > 1 else "single"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": measured_traffic(),
-                         "kernel": "mx_cast_kernel<fused2d>",
-                         "avg_launch_us": 1e6 * avg_launch},
+                         "traffic": measured_traffic() if R.name == "fused" and not args.shape
+                         and not args.workload else None,
+                         "kernel": R.kernel, "avg_launch_us": 1e6 * avg_launch,
+                         "launch_samples": len(per_launch)},
             "frac_of_peak": value / ws / peak,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": R.launches * args.steps,
             "clocks": clock_info,
         }
         print(json.dumps(line), flush=True)
@@ -377,7 +468,11 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--shape", type=int, nargs=2, metavar=("M", "K"), default=None,
-                   help="cast an M x K matrix of the same value mix instead (profiling)")
+                   help="fused / dim1: an M x K matrix of the same value mix instead; "
+                        "blocked: the R x C scale matrix")
+    p.add_argument("--row", choices=["fused", "dim1", "grouped", "experts", "blocked"],
+                   default="fused", help="which row of the hot path one step runs")
+    p.add_argument("--workload", default=None, help="named workload for the row")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
