@@ -258,39 +258,74 @@ __device__ __forceinline__ uint32_t dim1_unit(const uint8_t* in, uint8_t* q1s, u
 #undef MX_COL4_LO
 #undef MX_COL4_HI
 
+// Bytes s .. s+15 of the 32-byte window (a, b), s in 1..16 (byte s of a is
+// the window's byte s).  The word offset s >> 2 is uniform across the eight
+// lanes of a row, so the switch does not diverge within a row.
+__device__ __forceinline__ uint4 window16(const uint4& a, const uint4& b, int s) {
+  uint32_t x0, x1, x2, x3, x4;
+  switch (s >> 2) {
+    case 0: x0 = a.x; x1 = a.y; x2 = a.z; x3 = a.w; x4 = b.x; break;
+    case 1: x0 = a.y; x1 = a.z; x2 = a.w; x3 = b.x; x4 = b.y; break;
+    case 2: x0 = a.z; x1 = a.w; x2 = b.x; x3 = b.y; x4 = b.z; break;
+    case 3: x0 = a.w; x1 = b.x; x2 = b.y; x3 = b.z; x4 = b.w; break;
+    default: x0 = b.x; x1 = b.y; x2 = b.z; x3 = b.w; x4 = 0u; break;
+  }
+  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
+  uint4 o;
+  o.x = __funnelshift_r(x0, x1, r);
+  o.y = __funnelshift_r(x1, x2, r);
+  o.z = __funnelshift_r(x2, x3, r);
+  o.w = __funnelshift_r(x3, x4, r);
+  return o;
+}
+
+// One 16-byte aligned chunk j (0..8) of a q1 row segment that starts `delta`
+// bytes into its first chunk and holds `len` bytes from the staged row `srow`
+// (swizzle `sw`).  Full chunks take one vector store; the partial chunks at
+// the two ends are written byte by byte (their other bytes belong to the
+// neighbouring tiles).
+__device__ __forceinline__ void q1_chunk(const uint8_t* srow, int sw, uint8_t* gchunk, int j,
+                                         int delta, int len) {
+  const int o = 16 * j - delta;                    // local offset of the chunk's byte 0
+  const int b_lo = o < 0 ? -o : 0;
+  const int b_hi = (len - o) < 16 ? (len - o) : 16;
+  if (b_lo >= b_hi) return;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const uint4 a = (j >= 1 && j <= 8) ? *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4)) : zero;
+  const uint4 b = (j <= 7) ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : zero;
+  const uint4 v = window16(a, b, 16 - delta);
+  if (b_lo == 0 && b_hi == 16) {
+    *reinterpret_cast<uint4*>(gchunk) = v;
+  } else {
+#pragma unroll 1
+    for (int i = b_lo; i < b_hi; ++i) {
+      const uint32_t w = i < 8 ? (i < 4 ? v.x : v.y) : (i < 12 ? v.z : v.w);
+      gchunk[i] = static_cast<uint8_t>(w >> (8 * (i & 3)));
+    }
+  }
+}
+
 // Grouped mode: copy the staged q1 tile (128 columns of X = 128 rows of q1,
-// `len` valid bytes each) to q1 at row k0 + c, column m0.  Group starts need
-// not be aligned, so each warp writes one q1 row per step as 4-byte words
-// (128 contiguous bytes per step), with byte stores at the ragged ends.
+// `len` valid bytes each) to q1 row k0 + c, columns m0 .. m0 + len - 1.  Group
+// starts need not be aligned, so every row segment is written as the 16-byte
+// aligned chunks of q1 it covers (at most 9).  A warp takes four rows per
+// pass, eight lanes per row (128 contiguous bytes per row and store); lane 0
+// of a row also takes its ninth chunk.
 __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* q1, int64_t M, int64_t K,
                                             int m0, int k0, int len, int warp, int lane) {
-  for (int c = warp; c < kTile; c += kComputeWarps) {
+  const int j = lane & 7;
+#pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const int c = (warp * 4 + pass) * 4 + (lane >> 3);
     const int64_t kk = static_cast<int64_t>(k0) + c;
-    if (kk >= K) break;
-    const int64_t A = kk * M + m0;                 // byte offset of the row segment
-    const int al = static_cast<int>(A & 3);
-    const int64_t w0 = A >> 2;
-    const int nw = static_cast<int>(((A + len + 3) >> 2) - w0);
-    const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
-    const int sw = (c >> 1) & 7;
-    for (int j = lane; j < nw; j += 32) {
-      const int l0 = al ? j - 1 : j;               // staging word holding the first byte
-      uint32_t x0 = 0u, x1 = 0u;
-      if (l0 >= 0 && l0 < 32)
-        x0 = *reinterpret_cast<const uint32_t*>(srow + (((l0 >> 2) ^ sw) << 4) + (l0 & 3) * 4);
-      if (al && l0 + 1 < 32)
-        x1 = *reinterpret_cast<const uint32_t*>(srow + ((((l0 + 1) >> 2) ^ sw) << 4) +
-                                                ((l0 + 1) & 3) * 4);
-      const uint32_t val = al ? __funnelshift_r(x0, x1, 8 * (4 - al)) : x0;
-      const int o = 4 * j - al;                    // local offset of the word's byte 0
-      const int b_lo = o < 0 ? -o : 0;
-      const int b_hi = (len - o) < 4 ? (len - o) : 4;
-      uint8_t* g = q1 + ((w0 + j) << 2);
-      if (b_lo == 0 && b_hi == 4) {
-        *reinterpret_cast<uint32_t*>(g) = val;
-      } else {
-        for (int b = b_lo; b < b_hi; ++b) g[b] = static_cast<uint8_t>(val >> (8 * b));
-      }
+    if (kk < K) {
+      const int64_t A = kk * M + m0;                 // byte offset of the row segment
+      const int delta = static_cast<int>(A & 15);
+      uint8_t* g = q1 + (A - delta);                 // its first 16-byte chunk
+      const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
+      const int sw = (c >> 1) & 7;
+      q1_chunk(srow, sw, g + 16 * j, j, delta, len);
+      if (j == 0) q1_chunk(srow, sw, g + 128, 8, delta, len);
     }
   }
 }
