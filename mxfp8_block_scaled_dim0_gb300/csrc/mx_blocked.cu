@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(1024) group_offsets_kernel(const int32_t* __re
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
+  // The cast kernel that follows is launched as a programmatic dependent of
+  // this one; let it start its set-up now (it waits for this grid's results).
+  asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     carry_sh = 0;
     bad_sh = 0;

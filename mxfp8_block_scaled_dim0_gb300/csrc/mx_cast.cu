@@ -63,7 +63,11 @@ constexpr int kOffIn = 0;
 constexpr int kOffQ1 = kOffIn + kStages * kInBytes;
 constexpr int kOffS0 = kOffQ1 + kStaging * kQBytes;
 constexpr int kOffS1 = kOffS0 + kStaging * kScaleTile;
-constexpr int kOffBar = kOffS1 + kStaging * kScaleTile;
+constexpr int kOffCarry = kOffS1 + kStaging * kScaleTile;   // grouped: 128 x 16 B
+constexpr int kMaxSmemGroups = 1024;                         // group table cached in smem
+constexpr int kOffGTab = kOffCarry + kTile * 16;
+constexpr int kGTabBytes = ((2 * kMaxSmemGroups + 1) * 4 + 127) / 128 * 128;
+constexpr int kOffBar = kOffGTab + kGTabBytes;
 constexpr int kNumBars = 2 * kStages + 3 * kStaging;
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
@@ -77,7 +81,8 @@ struct Tile {
   int32_t m0;       // first row of X
   int32_t k0;       // first column of X
   int32_t rows;     // rows of the tile that belong to it (grouped mode), else 128
-  int32_t pad_;
+  int32_t cont;     // grouped: bit 0 = previous tile of this CTA is the one above in
+                    // the same column strip, bit 1 = next tile is the one below
   uint8_t* s0_dst;  // 512-byte blocked tile for dim0 scales
   uint8_t* s1_dst;  // 512-byte blocked tile for dim1 scales (null: scattered)
 };
@@ -103,35 +108,56 @@ struct Params {
   int32_t k128;             // ceil128(K)
 };
 
+// Group table of the grouped mode: tr[g] = padded tile-rows before group g
+// (s0_row_offs[g] / 128), ends[g] = offs[g].  Cached in shared memory when
+// G <= kMaxSmemGroups, else read from global memory.
+struct GroupTab {
+  const int32_t* tr_s;      // smem copy or null
+  const int32_t* ends_s;
+  const int64_t* row_offs;  // global
+  const int32_t* ends;
+  __device__ __forceinline__ int64_t tr(int g) const {
+    return tr_s ? static_cast<int64_t>(tr_s[g]) : (row_offs[g] >> 7);
+  }
+  __device__ __forceinline__ int64_t end(int g) const {
+    return ends_s ? static_cast<int64_t>(ends_s[g]) : static_cast<int64_t>(ends[g]);
+  }
+};
+
 __device__ __forceinline__ int64_t grouped_tiles(const Params& p) {
   return (p.row_offs[p.G] >> 7) * p.n_kt;
 }
 
+// Tile t of the launch.  2D / 3D modes: row-major over (M tiles, K tiles).
+// Grouped mode: ordered by group, then K tile, then M tile within the group,
+// so that a CTA's contiguous run of tiles walks down one column strip of a
+// group (this lets q1 rows be written in whole 16-byte chunks, see
+// copy_out_q1).
 template <int kMode>
-__device__ __forceinline__ Tile get_tile(const Params& p, int64_t t) {
+__device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, int64_t t) {
   Tile T;
-  T.pad_ = 0;
+  T.cont = 0;
   if (kMode == kModeGrouped) {
-    const int64_t R = t / p.n_kt;                  // padded tile-row
-    const int32_t tk = static_cast<int32_t>(t - R * p.n_kt);
-    const int64_t v = R << 7;
-    int lo = 0, hi = p.G;                          // row_offs[lo] <= v < row_offs[hi]
+    int lo = 0, hi = p.G;                          // tr(lo)*n_kt <= t < tr(hi)*n_kt
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (p.row_offs[mid] <= v) lo = mid; else hi = mid;
+      if (tab.tr(mid) * p.n_kt <= t) lo = mid; else hi = mid;
     }
     const int g = lo;
-    const int64_t t_in_g = R - (p.row_offs[g] >> 7);
-    const int64_t n_tg = (p.row_offs[g + 1] - p.row_offs[g]) >> 7;
-    const int64_t start = g ? p.offs[g - 1] : 0;
-    const int64_t m0 = start + (t_in_g << 7);
-    const int64_t left = static_cast<int64_t>(p.offs[g]) - m0;
+    const int64_t tr_g = tab.tr(g);
+    const int64_t n_tg = tab.tr(g + 1) - tr_g;
+    const int64_t v = t - tr_g * p.n_kt;
+    const int64_t tk = v / n_tg;
+    const int64_t tm = v - tk * n_tg;             // tile index within the group
+    const int64_t start = g ? tab.end(g - 1) : 0;
+    const int64_t m0 = start + (tm << 7);
+    const int64_t left = tab.end(g) - m0;
     T.m0 = static_cast<int32_t>(m0);
-    T.k0 = tk * kTile;
+    T.k0 = static_cast<int32_t>(tk * kTile);
     T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
-    T.s0_dst = p.s0 + (R * p.n_kt + tk) * kScaleTile;
-    T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (p.row_offs[g] >> 5) +
-               (tk * n_tg + t_in_g) * kScaleTile;
+    T.cont = (tm > 0 ? 1 : 0) | (tm + 1 < n_tg ? 2 : 0);
+    T.s0_dst = p.s0 + ((tr_g + tm) * p.n_kt + tk) * kScaleTile;
+    T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (tr_g * 4) + (tk * n_tg + tm) * kScaleTile;
   } else {
     const int32_t tm = static_cast<int32_t>(t / p.n_kt);
     const int32_t tk = static_cast<int32_t>(t - static_cast<int64_t>(tm) * p.n_kt);
@@ -279,53 +305,104 @@ __device__ __forceinline__ uint4 window16(const uint4& a, const uint4& b, int s)
   return o;
 }
 
-// One 16-byte aligned chunk j (0..8) of a q1 row segment that starts `delta`
-// bytes into its first chunk and holds `len` bytes from the staged row `srow`
-// (swizzle `sw`).  Full chunks take one vector store; the partial chunks at
-// the two ends are written byte by byte (their other bytes belong to the
-// neighbouring tiles).
-__device__ __forceinline__ void q1_chunk(const uint8_t* srow, int sw, uint8_t* gchunk, int j,
-                                         int delta, int len) {
-  const int o = 16 * j - delta;                    // local offset of the chunk's byte 0
-  const int b_lo = o < 0 ? -o : 0;
-  const int b_hi = (len - o) < 16 ? (len - o) : 16;
-  if (b_lo >= b_hi) return;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  const uint4 a = (j >= 1 && j <= 8) ? *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4)) : zero;
-  const uint4 b = (j <= 7) ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : zero;
-  const uint4 v = window16(a, b, 16 - delta);
-  if (b_lo == 0 && b_hi == 16) {
-    *reinterpret_cast<uint4*>(gchunk) = v;
-  } else {
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
+  return k < 2 ? (k == 0 ? v.x : v.y) : (k == 2 ? v.z : v.w);
+}
+
+// Bytes [lo, hi) of v to the 16-byte aligned address g (+lo ...), as the
+// fewest naturally aligned 8 / 4 / 2 / 1-byte stores (at most 7 for a
+// partial chunk).
+__device__ __forceinline__ void store_partial(uint8_t* g, const uint4& v, int lo, int hi) {
+  int i = lo;
 #pragma unroll 1
-    for (int i = b_lo; i < b_hi; ++i) {
-      const uint32_t w = i < 8 ? (i < 4 ? v.x : v.y) : (i < 12 ? v.z : v.w);
-      gchunk[i] = static_cast<uint8_t>(w >> (8 * (i & 3)));
+  while (i < hi) {
+    if ((i & 7) == 0 && i + 8 <= hi) {
+      *reinterpret_cast<uint2*>(g + i) = i == 0 ? make_uint2(v.x, v.y) : make_uint2(v.z, v.w);
+      i += 8;
+    } else if ((i & 3) == 0 && i + 4 <= hi) {
+      *reinterpret_cast<uint32_t*>(g + i) = word_of(v, i >> 2);
+      i += 4;
+    } else if ((i & 1) == 0 && i + 2 <= hi) {
+      *reinterpret_cast<uint16_t*>(g + i) = static_cast<uint16_t>(word_of(v, i >> 2) >> (8 * (i & 3)));
+      i += 2;
+    } else {
+      g[i] = static_cast<uint8_t>(word_of(v, i >> 2) >> (8 * (i & 3)));
+      i += 1;
     }
   }
 }
 
+// The 16 bytes that chunk j (0..8) of a row segment takes from the staged row
+// `srow` (swizzle `sw`) when the segment starts `delta` bytes into its first
+// chunk.
+__device__ __forceinline__ uint4 chunk_value(const uint8_t* srow, int sw, int j, int delta) {
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const uint4 a = (j >= 1 && j <= 8) ? *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4)) : zero;
+  const uint4 b = (j <= 7) ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : zero;
+  return window16(a, b, 16 - delta);
+}
+
 // Grouped mode: copy the staged q1 tile (128 columns of X = 128 rows of q1,
-// `len` valid bytes each) to q1 row k0 + c, columns m0 .. m0 + len - 1.  Group
-// starts need not be aligned, so every row segment is written as the 16-byte
-// aligned chunks of q1 it covers (at most 9).  A warp takes four rows per
-// pass, eight lanes per row (128 contiguous bytes per row and store); lane 0
-// of a row also takes its ninth chunk.
-__device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* q1, int64_t M, int64_t K,
-                                            int m0, int k0, int len, int warp, int lane) {
+// `len` valid bytes each) to q1 row k0 + c, columns m0 .. m0 + len - 1.
+// Group starts need not be aligned, so each row segment covers up to nine
+// 16-byte aligned chunks of q1, the first and last partial.  Within a CTA's
+// run down one column strip, the segment of the next tile starts exactly
+// where this one ends, so the partial last chunk is kept in `carry` (16 bytes
+// per row, shared memory) and completed by the next tile's partial first
+// chunk: nearly every store is a whole 16-byte chunk.  Only where a strip
+// starts or ends (group edges, the ends of a CTA's run) are partial chunks
+// stored piecewise.
+// A warp takes four rows per pass, eight lanes per row (128 contiguous bytes
+// per row and store); lane 0 of a row also takes the ninth chunk.
+__device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, uint8_t* q1,
+                                            int64_t M, int64_t K, int m0, int k0, int len,
+                                            bool cont_prev, bool cont_next, int warp, int lane) {
   const int j = lane & 7;
 #pragma unroll
   for (int pass = 0; pass < 4; ++pass) {
     const int c = (warp * 4 + pass) * 4 + (lane >> 3);
     const int64_t kk = static_cast<int64_t>(k0) + c;
-    if (kk < K) {
-      const int64_t A = kk * M + m0;                 // byte offset of the row segment
-      const int delta = static_cast<int>(A & 15);
-      uint8_t* g = q1 + (A - delta);                 // its first 16-byte chunk
-      const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
-      const int sw = (c >> 1) & 7;
-      q1_chunk(srow, sw, g + 16 * j, j, delta, len);
-      if (j == 0) q1_chunk(srow, sw, g + 128, 8, delta, len);
+    if (kk >= K) continue;
+    const int64_t A = kk * M + m0;                   // byte offset of the row segment
+    const int delta = static_cast<int>(A & 15);
+    uint8_t* g = q1 + (A - delta);                   // its first 16-byte chunk
+    const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
+    const int sw = (c >> 1) & 7;
+    uint4* cslot = reinterpret_cast<uint4*>(carry + c * 16);
+
+    // chunk j: local bytes [16j - delta, 16j - delta + 16) of the segment
+    const int o = 16 * j - delta;
+    const int b_lo = o < 0 ? -o : 0;
+    const int b_hi = (len - o) < 16 ? (len - o) : 16;
+    if (b_lo < b_hi) {
+      uint4 v = chunk_value(srow, sw, j, delta);
+      int lo = b_lo;
+      if (j == 0 && delta > 0 && cont_prev) {
+        // complete the previous tile's partial last chunk (its bytes [0, delta))
+        const uint4 prev = *cslot;
+        uint4 merged;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int nb = delta - 4 * k;              // carried bytes in word k
+          const uint32_t keep = nb >= 4 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : (0xFFFFFFFFu >> (8 * (4 - nb))));
+          const uint32_t w = (word_of(prev, k) & keep) | (word_of(v, k) & ~keep);
+          if (k == 0) merged.x = w; else if (k == 1) merged.y = w; else if (k == 2) merged.z = w; else merged.w = w;
+        }
+        v = merged;
+        lo = 0;
+      }
+      if (lo == 0 && b_hi == 16) *reinterpret_cast<uint4*>(g + 16 * j) = v;
+      else store_partial(g + 16 * j, v, lo, b_hi);
+    }
+    if (j == 0) {
+      // chunk 8: the segment's last `delta` bytes when it is a whole 128 bytes
+      const int o8 = 128 - delta;
+      const int hi8 = (len - o8) < 16 ? (len - o8) : 16;
+      if (hi8 > 0) {
+        const uint4 v8 = chunk_value(srow, sw, 8, delta);
+        if (cont_next) *cslot = v8;                  // finished by the next tile
+        else store_partial(g + 128, v8, 0, hi8);
+      }
     }
   }
 }
@@ -352,12 +429,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  int64_t n_tiles;
+  GroupTab tab = {nullptr, nullptr, p.row_offs, p.offs};
+  int64_t first, end, step;
   if (kMode == kModeGrouped) {
+    // The offsets come from the preceding group_offsets_kernel, launched as
+    // this kernel's programmatic prerequisite: wait for it before reading.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (*p.status != 0) return;               // invalid group offsets: write nothing
-    n_tiles = grouped_tiles(p);
+    const int64_t n_tiles = grouped_tiles(p);
+    // contiguous, balanced runs of tiles per CTA
+    first = n_tiles * blockIdx.x / gridDim.x;
+    end = n_tiles * (blockIdx.x + 1) / gridDim.x;
+    step = 1;
+    if (p.G <= kMaxSmemGroups) {
+      int32_t* tr_s = reinterpret_cast<int32_t*>(smem + kOffGTab);
+      int32_t* ends_s = tr_s + kMaxSmemGroups + 1;
+      for (int g = threadIdx.x; g <= p.G; g += blockDim.x) {
+        tr_s[g] = static_cast<int32_t>(p.row_offs[g] >> 7);
+        if (g < p.G) ends_s[g] = p.offs[g];
+      }
+      tab.tr_s = tr_s;
+      tab.ends_s = ends_s;
+    }
   } else {
-    n_tiles = p.n_tiles;
+    first = blockIdx.x;
+    end = p.n_tiles;
+    step = gridDim.x;
   }
 
   if (threadIdx.x == 0) {
@@ -375,18 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  const int64_t first = blockIdx.x;
-  const int64_t step = gridDim.x;
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tmap(&tm_x);
       int64_t it = 0;
-      for (int64_t t = first; t < n_tiles; t += step, ++it) {
+      for (int64_t t = first; t < end; t += step, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
-        const Tile T = get_tile<kMode>(p, t);
+        const Tile T = get_tile<kMode>(p, tab, t);
         uint8_t* dst = smem + kOffIn + s * kInBytes;
         mbar_arrive_expect_tx(&full[s], kInBytes);
         tma_load_2d(dst, &tm_x, T.k0, T.m0, &full[s]);
@@ -400,12 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q1o);
     }
     int64_t it = 0;
-    for (int64_t t = first; t < n_tiles; t += step, ++it) {
+    for (int64_t t = first; t < end; t += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
       const bool ok = mbar_wait(&sfull[o], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const Tile T = get_tile<kMode>(p, t);
+      const Tile T = get_tile<kMode>(p, tab, t);
       if (lane == 0) {
         if (kTmaQ1) {
           tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes);
@@ -441,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // compute warps
     int64_t it = 0;
-    for (int64_t t = first; t < n_tiles; t += step, ++it) {
+    for (int64_t t = first; t < end; t += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
       const int o = static_cast<int>(it % kStaging);
@@ -450,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = ok && mbar_wait(&sempty[o], oph ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
 
-      const Tile T = get_tile<kMode>(p, t);
+      const Tile T = get_tile<kMode>(p, tab, t);
       const uint8_t* in = smem + kOffIn + s * kInBytes;
       uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
       uint8_t* sc1 = smem + kOffS1 + o * kScaleTile;
@@ -495,7 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&qstaged[o]);
         const bool staged = mbar_wait(&qstaged[o], oph, abort_flag);
         if (!__all_sync(0xffffffffu, staged)) break;
-        copy_out_q1(q1s, p.q1, p.M, p.K, T.m0, T.k0, T.rows, warp, lane);
+        copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows,
+                    (T.cont & 1) && t > first, (T.cont & 2) && t + 1 < end, warp, lane);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -538,6 +634,22 @@ template <int kMode>
 int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t stream) {
   static int attr_rc = set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>));
   if (attr_rc != 0) return attr_rc;
+  if (kMode == kModeGrouped) {
+    // Programmatic dependent launch: the CTAs may start (barrier set-up) while
+    // group_offsets_kernel finishes; they wait for it before reading offsets.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return static_cast<int>(cudaLaunchKernelEx(&cfg, mx_cast_kernel<kMode>, maps.x, maps.q1e,
+                                               maps.q1o, prm));
+  }
   mx_cast_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(maps.x, maps.q1e, maps.q1o, prm);
   return static_cast<int>(cudaGetLastError());
 }

@@ -300,6 +300,15 @@ def test_grouped_random_sizes_many_groups():
     compare_grouped(W.spiky(M, K, 8, scale_frac=0.03, zero_frac=0.03), offs)
 
 
+@pytest.mark.parametrize("M,K,G,seed", [(9999, 1024, 5, 31), (16000, 512, 9, 32), (4097, 2048, 3, 33)])
+def test_grouped_multi_tile_runs(M, K, G, seed):
+    """Enough tiles that every CTA walks several tiles down a column strip, so
+    partial 16-byte chunks of q1 are carried from tile to tile; odd M makes
+    the misalignment differ from one q1 row to the next; some groups empty."""
+    offs = W.group_ends(M, G, seed, min_size=0).tolist()
+    compare_grouped(W.wide(M, K, seed, zero_frac=0.005), offs)
+
+
 def test_grouped_moe_workload_full():
     """The 16640 x 5120, 4-group MoE workload, every byte."""
     w = W.make("moe16640x5120_g4")
