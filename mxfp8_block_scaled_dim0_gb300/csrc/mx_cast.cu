@@ -25,7 +25,9 @@
 //              128B swizzle) into a kStages-deep ring
 //   warp 9     storer: TMA stores of the staged q1 tile, bulk copy of the
 //              dim0 scale tile, and the dim1 scale tile (staged in plain
-//              order, transposed to the blocked order on the way out)
+//              order, transposed to the blocked order on the way out);
+//              grouped mode: warps 9-12, which also copy q1 out with plain
+//              stores (group starts are not 16-byte aligned)
 // The depths were chosen by measurement on GB300: few input stages and many
 // output staging buffers.  More loads in flight (4-5 stages) slowed the
 // kernel by ~12%: outstanding writes, not reads, limit the mixed stream.
@@ -53,9 +55,8 @@ constexpr int kStages = 3;                 // input ring depth
 constexpr int kStaging = 6;                // q1 / scale staging buffers
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kThreads = kComputeThreads + 64;
 constexpr int kProducerWarp = kComputeWarps;
-constexpr int kStoreWarp = kComputeWarps + 1;
+constexpr int kFirstStoreWarp = kComputeWarps + 1;
 
 // Shared-memory layout, offsets from a 1024-byte aligned base (the 128B
 // swizzle pattern repeats every 1024 bytes).
@@ -68,7 +69,7 @@ constexpr int kMaxSmemGroups = 1024;                         // group table cach
 constexpr int kOffGTab = kOffCarry + kTile * 16;
 constexpr int kGTabBytes = ((2 * kMaxSmemGroups + 1) * 4 + 127) / 128 * 128;
 constexpr int kOffBar = kOffGTab + kGTabBytes;
-constexpr int kNumBars = 2 * kStages + 3 * kStaging;
+constexpr int kNumBars = 2 * kStages + 2 * kStaging;
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -76,6 +77,15 @@ constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 enum Mode : int { kModeFused2D = 0, kModeDim1 = 1, kModeExperts = 2, kModeGrouped = 3 };
+
+// One store warp drains a staging buffer by TMA in the 2D / 3D modes.  In
+// the grouped mode q1 cannot leave by TMA (group starts are not 16-byte
+// aligned), so four store warps copy it out with plain stores, off the
+// compute warps' path.
+__host__ __device__ constexpr int store_warps(int mode) { return mode == kModeGrouped ? 4 : 1; }
+__host__ __device__ constexpr int threads_of(int mode) {
+  return (kComputeWarps + 1 + store_warps(mode)) * 32;
+}
 
 struct Tile {
   int32_t m0;       // first row of X
@@ -352,15 +362,17 @@ __device__ __forceinline__ uint4 chunk_value(const uint8_t* srow, int sw, int j,
 // chunk: nearly every store is a whole 16-byte chunk.  Only where a strip
 // starts or ends (group edges, the ends of a CTA's run) are partial chunks
 // stored piecewise.
-// A warp takes four rows per pass, eight lanes per row (128 contiguous bytes
-// per row and store); lane 0 of a row also takes the ninth chunk.
+// Store warp `sw` (0..3) takes rows 32*sw .. 32*sw+31, four rows per pass,
+// eight lanes per row (128 contiguous bytes per row and store); lane 0 of a
+// row also takes the ninth chunk.  A row is always handled by the same lane,
+// so its carried chunk needs no synchronisation.
 __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, uint8_t* q1,
                                             int64_t M, int64_t K, int m0, int k0, int len,
-                                            bool cont_prev, bool cont_next, int warp, int lane) {
+                                            bool cont_prev, bool cont_next, int sw_idx, int lane) {
   const int j = lane & 7;
-#pragma unroll
-  for (int pass = 0; pass < 4; ++pass) {
-    const int c = (warp * 4 + pass) * 4 + (lane >> 3);
+#pragma unroll 2
+  for (int pass = 0; pass < 8; ++pass) {
+    const int c = 32 * sw_idx + pass * 4 + (lane >> 3);
     const int64_t kk = static_cast<int64_t>(k0) + c;
     if (kk >= K) continue;
     const int64_t A = kk * M + m0;                   // byte offset of the row segment
@@ -410,7 +422,7 @@ __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, 
 // ---- the kernel -------------------------------------------------------------
 
 template <int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(kMode), 1)
     mx_cast_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q1e,
                    const __grid_constant__ CUtensorMap tm_q1o, const Params p) {
   constexpr bool kDim0 = (kMode == kModeFused2D || kMode == kModeGrouped);
@@ -423,7 +435,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = bars + kStages;           // [kStages] compute done reading
   uint64_t* sfull = bars + 2 * kStages;       // [kStaging] staging written
   uint64_t* sempty = sfull + kStaging;        // [kStaging] staging drained
-  uint64_t* qstaged = sfull + 2 * kStaging;   // [kStaging] grouped: q1 staged
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
 
   const int warp = threadIdx.x >> 5;
@@ -464,8 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int o = 0; o < kStaging; ++o) {
       mbar_init(&sfull[o], kComputeWarps);
-      mbar_init(&sempty[o], 1);
-      mbar_init(&qstaged[o], kComputeWarps);
+      mbar_init(&sempty[o], store_warps(kMode));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -489,8 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kStoreWarp) {
-    if (lane == 0 && kTmaQ1) {
+  } else if (warp >= kFirstStoreWarp) {
+    const int sw = warp - kFirstStoreWarp;
+    if (sw == 0 && lane == 0 && kTmaQ1) {
       prefetch_tmap(&tm_q1e);
       prefetch_tmap(&tm_q1o);
     }
@@ -501,37 +512,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = mbar_wait(&sfull[o], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       const Tile T = get_tile<kMode>(p, tab, t);
-      if (lane == 0) {
-        if (kTmaQ1) {
-          tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes);
-          tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes + kQ1Half);
+      if (sw == 0) {
+        if (lane == 0) {
+          if (kTmaQ1) {
+            tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes);
+            tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes + kQ1Half);
+          }
+          if (kDim0) bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
+          bulk_commit();
         }
-        if (kDim0) bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
-        bulk_commit();
-      }
-      if (T.s1_dst) {
-        // dim1 scales are staged as [M-block][column]; storage row `lane` of
-        // the blocked tile holds columns lane, lane+32, lane+64, lane+96, four
-        // M-blocks each.
-        const uint8_t* nat = smem + kOffS1 + o * kScaleTile;
-        uint4 w;
-        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+        if (T.s1_dst) {
+          // dim1 scales are staged as [M-block][column]; storage row `lane` of
+          // the blocked tile holds columns lane, lane+32, lane+64, lane+96,
+          // four M-blocks each.
+          const uint8_t* nat = smem + kOffS1 + o * kScaleTile;
+          uint4 w;
+          uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          const int c = lane + 32 * a;
-          wp[a] = static_cast<uint32_t>(nat[c]) | (static_cast<uint32_t>(nat[128 + c]) << 8) |
-                  (static_cast<uint32_t>(nat[256 + c]) << 16) |
-                  (static_cast<uint32_t>(nat[384 + c]) << 24);
+          for (int a = 0; a < 4; ++a) {
+            const int c = lane + 32 * a;
+            wp[a] = static_cast<uint32_t>(nat[c]) | (static_cast<uint32_t>(nat[128 + c]) << 8) |
+                    (static_cast<uint32_t>(nat[256 + c]) << 16) |
+                    (static_cast<uint32_t>(nat[384 + c]) << 24);
+          }
+          *reinterpret_cast<uint4*>(T.s1_dst + lane * 16) = w;
         }
-        *reinterpret_cast<uint4*>(T.s1_dst + lane * 16) = w;
       }
+      if (kMode == kModeGrouped)
+        copy_out_q1(smem + kOffQ1 + o * kQBytes, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0,
+                    T.rows, (T.cont & 1) && t > first, (T.cont & 2) && t + 1 < end, sw, lane);
       __syncwarp();
       if (lane == 0) {
-        bulk_wait_read<0>();
+        if (sw == 0) bulk_wait_read<0>();
         mbar_arrive(&sempty[o]);
       }
     }
-    if (lane == 0) bulk_wait<0>();
+    if (sw == 0 && lane == 0) bulk_wait<0>();
     __syncwarp();
   } else {
     // compute warps
@@ -582,17 +598,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);     // input stage may be refilled
 
-      if (kMode == kModeGrouped) {
-        // All compute warps must have staged q1 before any copies it out.  An
-        // mbarrier (bounded wait) rather than bar.sync, so that a CTA whose
-        // other warps stopped on the abort flag cannot hang here.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qstaged[o]);
-        const bool staged = mbar_wait(&qstaged[o], oph, abort_flag);
-        if (!__all_sync(0xffffffffu, staged)) break;
-        copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows,
-                    (T.cont & 1) && t > first, (T.cont & 2) && t + 1 < end, warp, lane);
-      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfull[o]);
@@ -639,7 +644,7 @@ int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t strea
     // group_offsets_kernel finishes; they wait for it before reading offsets.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads_of(kMode));
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -650,14 +655,15 @@ int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t strea
     return static_cast<int>(cudaLaunchKernelEx(&cfg, mx_cast_kernel<kMode>, maps.x, maps.q1e,
                                                maps.q1o, prm));
   }
-  mx_cast_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(maps.x, maps.q1e, maps.q1o, prm);
+  mx_cast_kernel<kMode><<<grid, threads_of(kMode), kSmemBytes, stream>>>(maps.x, maps.q1e, maps.q1o,
+                                                                          prm);
   return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace
 
 int smem_bytes_cast() { return kSmemBytes; }
-int threads_cast() { return kThreads; }
+int threads_cast() { return threads_of(kModeFused2D); }
 
 int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0, void* s1,
                    int num_sms, cudaStream_t stream) {
