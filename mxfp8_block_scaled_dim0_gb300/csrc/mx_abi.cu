@@ -191,8 +191,10 @@ int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, 
       !aligned(s1_col_offs, 8) || !aligned(status, 4))
     return MX_ERR_ALIGN;
   mx::CastMaps maps;
-  // q1 is written with plain stores (group starts are not 16-byte aligned).
-  if (int rc = encode_cast_maps(&maps, x, M, K, nullptr)) return rc;
+  // q1 rows are 16-byte aligned only when M % 16 == 0; then whole tiles may
+  // leave by TMA (see the grouped kernel), otherwise all of q1 is written with
+  // plain stores.
+  if (int rc = encode_cast_maps(&maps, x, M, K, M % 16 == 0 ? q1 : nullptr)) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

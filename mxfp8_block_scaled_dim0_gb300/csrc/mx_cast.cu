@@ -69,7 +69,7 @@ constexpr int kMaxSmemGroups = 1024;                         // group table cach
 constexpr int kOffGTab = kOffCarry + kTile * 16;
 constexpr int kGTabBytes = ((2 * kMaxSmemGroups + 1) * 4 + 127) / 128 * 128;
 constexpr int kOffBar = kOffGTab + kGTabBytes;
-constexpr int kNumBars = 2 * kStages + 2 * kStaging;
+constexpr int kNumBars = 2 * kStages + 3 * kStaging;
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -116,6 +116,8 @@ struct Params {
   const int32_t* status;
   int32_t G;
   int32_t k128;             // ceil128(K)
+  int32_t q1_tma;           // grouped: q1 rows 16-byte aligned (M % 16 == 0), so
+                            // whole 128-byte tiles may leave by TMA
 };
 
 // Group table of the grouped mode: tr[g] = padded tile-rows before group g
@@ -352,6 +354,48 @@ __device__ __forceinline__ uint4 chunk_value(const uint8_t* srow, int sw, int j,
   return window16(a, b, 16 - delta);
 }
 
+// Grouped mode, whole interior tile of a column strip: shift the staged q1
+// rows in place so that each row starts at its 16-byte aligned chunk, with the
+// first `delta` bytes taken from the previous tile's carried chunk and the
+// last `delta` bytes carried to the next tile.  The shifted tile is then one
+// aligned 128-byte TMA box per row.  Rows 32*sw_idx .. +31, eight lanes per
+// row; all lanes read before any writes (the shift is in place).
+__device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta, int sw_idx,
+                                              int lane) {
+  const int j = lane & 7;
+  uint4 v[8];
+#pragma unroll
+  for (int pass = 0; pass < 8; ++pass) {
+    const int c = 32 * sw_idx + pass * 4 + (lane >> 3);
+    const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
+    const int sw = (c >> 1) & 7;
+    v[pass] = chunk_value(srow, sw, j, delta);
+    uint4* cslot = reinterpret_cast<uint4*>(carry + c * 16);
+    if (j == 0) {
+      const uint4 prev = *cslot;
+      const uint4 next = chunk_value(srow, sw, 8, delta);
+      uint4 merged;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int nb = delta - 4 * k;                // carried bytes in word k
+        const uint32_t keep = nb >= 4 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : (0xFFFFFFFFu >> (8 * (4 - nb))));
+        const uint32_t w = (word_of(prev, k) & keep) | (word_of(v[pass], k) & ~keep);
+        if (k == 0) merged.x = w; else if (k == 1) merged.y = w; else if (k == 2) merged.z = w; else merged.w = w;
+      }
+      v[pass] = merged;
+      *cslot = next;
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int pass = 0; pass < 8; ++pass) {
+    const int c = 32 * sw_idx + pass * 4 + (lane >> 3);
+    uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
+    const int sw = (c >> 1) & 7;
+    *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = v[pass];
+  }
+}
+
 // Grouped mode: copy the staged q1 tile (128 columns of X = 128 rows of q1,
 // `len` valid bytes each) to q1 row k0 + c, columns m0 .. m0 + len - 1.
 // Group starts need not be aligned, so each row segment covers up to nine
@@ -435,6 +479,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   uint64_t* empty = bars + kStages;           // [kStages] compute done reading
   uint64_t* sfull = bars + 2 * kStages;       // [kStaging] staging written
   uint64_t* sempty = sfull + kStaging;        // [kStaging] staging drained
+  uint64_t* qdone = sfull + 2 * kStaging;     // [kStaging] grouped: store warps done
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
 
   const int warp = threadIdx.x >> 5;
@@ -475,7 +520,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     }
     for (int o = 0; o < kStaging; ++o) {
       mbar_init(&sfull[o], kComputeWarps);
-      mbar_init(&sempty[o], store_warps(kMode));
+      mbar_init(&sempty[o], 1);
+      mbar_init(&qdone[o], store_warps(kMode));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -501,7 +547,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     __syncwarp();
   } else if (warp >= kFirstStoreWarp) {
     const int sw = warp - kFirstStoreWarp;
-    if (sw == 0 && lane == 0 && kTmaQ1) {
+    if (sw == 0 && lane == 0 && (kTmaQ1 || p.q1_tma)) {
       prefetch_tmap(&tm_q1e);
       prefetch_tmap(&tm_q1o);
     }
@@ -512,11 +558,39 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       const bool ok = mbar_wait(&sfull[o], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       const Tile T = get_tile<kMode>(p, tab, t);
+      uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
+      bool q1_box = kTmaQ1;               // the staged q1 tile leaves as TMA boxes
+      int32_t box_x = T.m0;
+      if (kMode == kModeGrouped) {
+        // Grouped: a whole 128-row tile whose q1 rows are 16-byte aligned at
+        // a common offset leaves by TMA, shifted onto the aligned chunks when
+        // that offset is not 0 (which needs the carried chunk of the tile
+        // above and hands its own last chunk to the tile below).  All other
+        // tiles (strip ends, partial tiles, odd M) are stored piecewise.
+        const bool cont_prev = (T.cont & 1) && t > first;
+        const bool cont_next = (T.cont & 2) && t + 1 < end;
+        const int delta = T.m0 & 15;
+        q1_box = p.q1_tma && T.rows == kTile && (delta == 0 || (cont_prev && cont_next));
+        if (q1_box) {
+          if (delta != 0) shift_q1_rows(q1s, smem + kOffCarry, delta, sw, lane);
+          box_x = T.m0 - delta;
+          fence_proxy_async_smem();
+        } else {
+          copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows, cont_prev,
+                      cont_next, sw, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qdone[o]);
+      }
       if (sw == 0) {
+        if (kMode == kModeGrouped) {
+          const bool done = mbar_wait(&qdone[o], ph, abort_flag);
+          if (!__all_sync(0xffffffffu, done)) break;
+        }
         if (lane == 0) {
-          if (kTmaQ1) {
-            tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes);
-            tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, smem + kOffQ1 + o * kQBytes + kQ1Half);
+          if (q1_box) {
+            tma_store_2d(&tm_q1e, box_x, T.k0 >> 1, q1s);
+            tma_store_2d(&tm_q1o, box_x, T.k0 >> 1, q1s + kQ1Half);
           }
           if (kDim0) bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
           bulk_commit();
@@ -537,14 +611,11 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
           }
           *reinterpret_cast<uint4*>(T.s1_dst + lane * 16) = w;
         }
-      }
-      if (kMode == kModeGrouped)
-        copy_out_q1(smem + kOffQ1 + o * kQBytes, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0,
-                    T.rows, (T.cont & 1) && t > first, (T.cont & 2) && t + 1 < end, sw, lane);
-      __syncwarp();
-      if (lane == 0) {
-        if (sw == 0) bulk_wait_read<0>();
-        mbar_arrive(&sempty[o]);
+        __syncwarp();
+        if (lane == 0) {
+          bulk_wait_read<0>();
+          mbar_arrive(&sempty[o]);
+        }
       }
     }
     if (sw == 0 && lane == 0) bulk_wait<0>();
@@ -718,6 +789,7 @@ int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_
   prm.status = status;
   prm.G = G;
   prm.k128 = static_cast<int32_t>((K + 127) / 128 * 128);
+  prm.q1_tma = (M % 16) == 0;
   const int64_t bound = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
   const int grid = static_cast<int>(bound < num_sms ? (bound > 0 ? bound : 1) : num_sms);
   return launch<kModeGrouped>(maps, prm, grid, stream);
