@@ -296,27 +296,6 @@ __device__ __forceinline__ uint32_t dim1_unit(const uint8_t* in, uint8_t* q1s, u
 #undef MX_COL4_LO
 #undef MX_COL4_HI
 
-// Bytes s .. s+15 of the 32-byte window (a, b), s in 1..16 (byte s of a is
-// the window's byte s).  The word offset s >> 2 is uniform across the eight
-// lanes of a row, so the switch does not diverge within a row.
-__device__ __forceinline__ uint4 window16(const uint4& a, const uint4& b, int s) {
-  uint32_t x0, x1, x2, x3, x4;
-  switch (s >> 2) {
-    case 0: x0 = a.x; x1 = a.y; x2 = a.z; x3 = a.w; x4 = b.x; break;
-    case 1: x0 = a.y; x1 = a.z; x2 = a.w; x3 = b.x; x4 = b.y; break;
-    case 2: x0 = a.z; x1 = a.w; x2 = b.x; x3 = b.y; x4 = b.z; break;
-    case 3: x0 = a.w; x1 = b.x; x2 = b.y; x3 = b.z; x4 = b.w; break;
-    default: x0 = b.x; x1 = b.y; x2 = b.z; x3 = b.w; x4 = 0u; break;
-  }
-  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
-  uint4 o;
-  o.x = __funnelshift_r(x0, x1, r);
-  o.y = __funnelshift_r(x1, x2, r);
-  o.z = __funnelshift_r(x2, x3, r);
-  o.w = __funnelshift_r(x3, x4, r);
-  return o;
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int k) {
   return k < 2 ? (k == 0 ? v.x : v.y) : (k == 2 ? v.z : v.w);
 }
@@ -344,47 +323,56 @@ __device__ __forceinline__ void store_partial(uint8_t* g, const uint4& v, int lo
   }
 }
 
-// The 16 bytes that chunk j (0..8) of a row segment takes from the staged row
-// `srow` (swizzle `sw`) when the segment starts `delta` bytes into its first
-// chunk.
-__device__ __forceinline__ uint4 chunk_value(const uint8_t* srow, int sw, int j, int delta) {
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  const uint4 a = (j >= 1 && j <= 8) ? *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4)) : zero;
-  const uint4 b = (j <= 7) ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : zero;
-  return window16(a, b, 16 - delta);
+// Grouped mode, q1 rows.  A tile's q1 row segment (its 128 staged bytes)
+// starts `delta` bytes into a 16-byte chunk of q1 (group starts are not
+// aligned).  Chunk j (0..8) of the segment's aligned chunks holds bytes
+// [16j - delta, 16j - delta + 16) of the segment; bytes before 0 are the
+// previous tile's last bytes.  Those come from `cslot`, which holds the
+// previous tile's raw last 16 bytes (its carried chunk), so chunk j is bytes
+// [16j + 16 - delta, ...) of the extended row [cslot | staged row].  Read as
+// five 4-byte words and one funnel shift: no branches, no register indexing.
+__device__ __forceinline__ uint4 aligned_chunk(const uint8_t* srow, int sw, const uint8_t* cslot,
+                                               int j, int delta) {
+  const int e0 = 16 * j + 16 - delta;              // extended byte offset (1 .. 144)
+  const int w0 = e0 >> 2;
+  const uint32_t r = 8u * static_cast<uint32_t>(e0 & 3);
+  uint32_t w[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    const int we = w0 + i;                         // 0..3 carried chunk, 4..35 staged row
+    const int rw = we - 4;
+    const uint8_t* a = we < 4 ? cslot + 4 * we : srow + (((rw >> 2) ^ sw) << 4) + (rw & 3) * 4;
+    w[i] = we < 36 ? *reinterpret_cast<const uint32_t*>(a) : 0u;
+  }
+  uint4 o;
+  o.x = __funnelshift_r(w[0], w[1], r);
+  o.y = __funnelshift_r(w[1], w[2], r);
+  o.z = __funnelshift_r(w[2], w[3], r);
+  o.w = __funnelshift_r(w[3], w[4], r);
+  return o;
 }
 
-// Grouped mode, whole interior tile of a column strip: shift the staged q1
-// rows in place so that each row starts at its 16-byte aligned chunk, with the
-// first `delta` bytes taken from the previous tile's carried chunk and the
-// last `delta` bytes carried to the next tile.  The shifted tile is then one
-// aligned 128-byte TMA box per row.  Rows 32*sw_idx .. +31, eight lanes per
-// row; all lanes read before any writes (the shift is in place).
+__device__ __forceinline__ uint4 staged_chunk(const uint8_t* srow, int sw, int k) {
+  return *reinterpret_cast<const uint4*>(srow + ((k ^ sw) << 4));
+}
+
+// Grouped mode, whole interior tile of a column strip: rewrite the staged q1
+// rows in place onto their aligned chunks (chunk 0 completes the previous
+// tile's partial last chunk from the carried bytes), so that each row is one
+// 16-byte aligned 128-byte TMA box.  The row's raw last 16 bytes become the
+// carried chunk of the next tile.  Rows 32*sw_idx .. +31, eight lanes per row
+// (lane j takes chunk j); every read happens before any write.
 __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta, int sw_idx,
                                               int lane) {
   const int j = lane & 7;
-  uint4 v[8];
+  uint4 v[8], last[8];
 #pragma unroll
   for (int pass = 0; pass < 8; ++pass) {
     const int c = 32 * sw_idx + pass * 4 + (lane >> 3);
     const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
     const int sw = (c >> 1) & 7;
-    v[pass] = chunk_value(srow, sw, j, delta);
-    uint4* cslot = reinterpret_cast<uint4*>(carry + c * 16);
-    if (j == 0) {
-      const uint4 prev = *cslot;
-      const uint4 next = chunk_value(srow, sw, 8, delta);
-      uint4 merged;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int nb = delta - 4 * k;                // carried bytes in word k
-        const uint32_t keep = nb >= 4 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : (0xFFFFFFFFu >> (8 * (4 - nb))));
-        const uint32_t w = (word_of(prev, k) & keep) | (word_of(v[pass], k) & ~keep);
-        if (k == 0) merged.x = w; else if (k == 1) merged.y = w; else if (k == 2) merged.z = w; else merged.w = w;
-      }
-      v[pass] = merged;
-      *cslot = next;
-    }
+    v[pass] = aligned_chunk(srow, sw, carry + c * 16, j, delta);
+    last[pass] = staged_chunk(srow, sw, 7);
   }
   __syncwarp();
 #pragma unroll
@@ -393,23 +381,19 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
     uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
     const int sw = (c >> 1) & 7;
     *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = v[pass];
+    if (j == 0) *reinterpret_cast<uint4*>(carry + c * 16) = last[pass];
   }
 }
 
-// Grouped mode: copy the staged q1 tile (128 columns of X = 128 rows of q1,
-// `len` valid bytes each) to q1 row k0 + c, columns m0 .. m0 + len - 1.
-// Group starts need not be aligned, so each row segment covers up to nine
-// 16-byte aligned chunks of q1, the first and last partial.  Within a CTA's
-// run down one column strip, the segment of the next tile starts exactly
-// where this one ends, so the partial last chunk is kept in `carry` (16 bytes
-// per row, shared memory) and completed by the next tile's partial first
-// chunk: nearly every store is a whole 16-byte chunk.  Only where a strip
-// starts or ends (group edges, the ends of a CTA's run) are partial chunks
-// stored piecewise.
-// Store warp `sw` (0..3) takes rows 32*sw .. 32*sw+31, four rows per pass,
-// eight lanes per row (128 contiguous bytes per row and store); lane 0 of a
-// row also takes the ninth chunk.  A row is always handled by the same lane,
-// so its carried chunk needs no synchronisation.
+// Grouped mode, other tiles (strip ends, partial tiles, odd M): store the
+// staged q1 rows (`len` valid bytes each) to q1 row k0 + c, columns m0 ..
+// m0 + len - 1, as the aligned chunks they cover.  Whole chunks take one
+// vector store; a partial chunk (at a strip end, or where the tile above was
+// handled by another CTA) is stored piecewise.  When the tile below follows in
+// this CTA, the last chunk is not stored: it is completed there from the
+// carried raw last 16 bytes of this row.  Rows 32*sw_idx .. +31, eight lanes
+// per row (128 contiguous bytes per row and store); lane 0 of a row also takes
+// the ninth chunk and the carry.
 __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, uint8_t* q1,
                                             int64_t M, int64_t K, int m0, int k0, int len,
                                             bool cont_prev, bool cont_next, int sw_idx, int lane) {
@@ -421,44 +405,28 @@ __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, 
     if (kk >= K) continue;
     const int64_t A = kk * M + m0;                   // byte offset of the row segment
     const int delta = static_cast<int>(A & 15);
-    uint8_t* g = q1 + (A - delta);                   // its first 16-byte chunk
+    uint8_t* g = q1 + (A - delta);                   // its first aligned chunk
     const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
     const int sw = (c >> 1) & 7;
-    uint4* cslot = reinterpret_cast<uint4*>(carry + c * 16);
+    uint8_t* cslot = carry + c * 16;
 
-    // chunk j: local bytes [16j - delta, 16j - delta + 16) of the segment
+    // chunk j: segment bytes [16j - delta, 16j - delta + 16)
     const int o = 16 * j - delta;
-    const int b_lo = o < 0 ? -o : 0;
+    int b_lo = o < 0 ? -o : 0;
     const int b_hi = (len - o) < 16 ? (len - o) : 16;
+    if (j == 0 && cont_prev) b_lo = 0;               // the carried bytes complete it
     if (b_lo < b_hi) {
-      uint4 v = chunk_value(srow, sw, j, delta);
-      int lo = b_lo;
-      if (j == 0 && delta > 0 && cont_prev) {
-        // complete the previous tile's partial last chunk (its bytes [0, delta))
-        const uint4 prev = *cslot;
-        uint4 merged;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int nb = delta - 4 * k;              // carried bytes in word k
-          const uint32_t keep = nb >= 4 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : (0xFFFFFFFFu >> (8 * (4 - nb))));
-          const uint32_t w = (word_of(prev, k) & keep) | (word_of(v, k) & ~keep);
-          if (k == 0) merged.x = w; else if (k == 1) merged.y = w; else if (k == 2) merged.z = w; else merged.w = w;
-        }
-        v = merged;
-        lo = 0;
-      }
-      if (lo == 0 && b_hi == 16) *reinterpret_cast<uint4*>(g + 16 * j) = v;
-      else store_partial(g + 16 * j, v, lo, b_hi);
+      const uint4 v = aligned_chunk(srow, sw, cslot, j, delta);
+      if (b_lo == 0 && b_hi == 16) *reinterpret_cast<uint4*>(g + 16 * j) = v;
+      else store_partial(g + 16 * j, v, b_lo, b_hi);
     }
     if (j == 0) {
       // chunk 8: the segment's last `delta` bytes when it is a whole 128 bytes
       const int o8 = 128 - delta;
       const int hi8 = (len - o8) < 16 ? (len - o8) : 16;
-      if (hi8 > 0) {
-        const uint4 v8 = chunk_value(srow, sw, 8, delta);
-        if (cont_next) *cslot = v8;                  // finished by the next tile
-        else store_partial(g + 128, v8, 0, hi8);
-      }
+      if (hi8 > 0 && !cont_next)
+        store_partial(g + 128, aligned_chunk(srow, sw, cslot, 8, delta), 0, hi8);
+      if (cont_next) *reinterpret_cast<uint4*>(cslot) = staged_chunk(srow, sw, 7);
     }
   }
 }
