@@ -329,26 +329,36 @@ __device__ __forceinline__ void store_partial(uint8_t* g, const uint4& v, int lo
 // [16j - delta, 16j - delta + 16) of the segment; bytes before 0 are the
 // previous tile's last bytes.  Those come from `cslot`, which holds the
 // previous tile's raw last 16 bytes (its carried chunk), so chunk j is bytes
-// [16j + 16 - delta, ...) of the extended row [cslot | staged row].  Read as
-// five 4-byte words and one funnel shift: no branches, no register indexing.
+// [16 - delta, 32 - delta) of the 32-byte window (a, b) = (extended chunk j,
+// extended chunk j + 1) of the extended row [cslot | staged row].  Two
+// conflict-free 16-byte loads; the uniform word offset (16 - delta) / 4 is
+// applied with three levels of selects, the byte offset with funnel shifts.
 __device__ __forceinline__ uint4 aligned_chunk(const uint8_t* srow, int sw, const uint8_t* cslot,
                                                int j, int delta) {
-  const int e0 = 16 * j + 16 - delta;              // extended byte offset (1 .. 144)
-  const int w0 = e0 >> 2;
-  const uint32_t r = 8u * static_cast<uint32_t>(e0 & 3);
-  uint32_t w[5];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) {
-    const int we = w0 + i;                         // 0..3 carried chunk, 4..35 staged row
-    const int rw = we - 4;
-    const uint8_t* a = we < 4 ? cslot + 4 * we : srow + (((rw >> 2) ^ sw) << 4) + (rw & 3) * 4;
-    w[i] = we < 36 ? *reinterpret_cast<const uint32_t*>(a) : 0u;
-  }
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const uint4 a = j == 0 ? *reinterpret_cast<const uint4*>(cslot)
+                         : *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4));
+  const uint4 b = j <= 7 ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : zero;
+  const int s = 16 - delta;                          // 1 .. 16
+  const int q = s >> 2;                              // word offset 0 .. 4
+  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
+  // w[i] = window word q + i, i = 0..4 (window words 8.. are zero)
+  const uint32_t W0 = a.x, W1 = a.y, W2 = a.z, W3 = a.w, W4 = b.x, W5 = b.y, W6 = b.z, W7 = b.w;
+  const bool q1b = q & 1, q2b = q & 2, q4b = q & 4;
+  // shift by (q & 1)
+  const uint32_t t0 = q1b ? W1 : W0, t1 = q1b ? W2 : W1, t2 = q1b ? W3 : W2, t3 = q1b ? W4 : W3,
+                 t4 = q1b ? W5 : W4, t5 = q1b ? W6 : W5, t6 = q1b ? W7 : W6, t7 = q1b ? 0u : W7;
+  // shift by (q & 2)
+  const uint32_t u0 = q2b ? t2 : t0, u1 = q2b ? t3 : t1, u2 = q2b ? t4 : t2, u3 = q2b ? t5 : t3,
+                 u4 = q2b ? t6 : t4, u5 = q2b ? t7 : t5, u6 = q2b ? 0u : t6, u7 = q2b ? 0u : t7;
+  // shift by (q & 4)
+  const uint32_t x0 = q4b ? u4 : u0, x1 = q4b ? u5 : u1, x2 = q4b ? u6 : u2, x3 = q4b ? u7 : u3,
+                 x4 = q4b ? 0u : u4;
   uint4 o;
-  o.x = __funnelshift_r(w[0], w[1], r);
-  o.y = __funnelshift_r(w[1], w[2], r);
-  o.z = __funnelshift_r(w[2], w[3], r);
-  o.w = __funnelshift_r(w[3], w[4], r);
+  o.x = __funnelshift_r(x0, x1, r);
+  o.y = __funnelshift_r(x1, x2, r);
+  o.z = __funnelshift_r(x2, x3, r);
+  o.w = __funnelshift_r(x3, x4, r);
   return o;
 }
 
@@ -365,23 +375,26 @@ __device__ __forceinline__ uint4 staged_chunk(const uint8_t* srow, int sw, int k
 __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta, int sw_idx,
                                               int lane) {
   const int j = lane & 7;
-  uint4 v[8], last[8];
 #pragma unroll
-  for (int pass = 0; pass < 8; ++pass) {
-    const int c = 32 * sw_idx + pass * 4 + (lane >> 3);
-    const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
-    const int sw = (c >> 1) & 7;
-    v[pass] = aligned_chunk(srow, sw, carry + c * 16, j, delta);
-    last[pass] = staged_chunk(srow, sw, 7);
-  }
-  __syncwarp();
+  for (int half = 0; half < 2; ++half) {
+    uint4 v[4], last[4];
 #pragma unroll
-  for (int pass = 0; pass < 8; ++pass) {
-    const int c = 32 * sw_idx + pass * 4 + (lane >> 3);
-    uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
-    const int sw = (c >> 1) & 7;
-    *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = v[pass];
-    if (j == 0) *reinterpret_cast<uint4*>(carry + c * 16) = last[pass];
+    for (int pp = 0; pp < 4; ++pp) {
+      const int c = 32 * sw_idx + (4 * half + pp) * 4 + (lane >> 3);
+      const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
+      const int sw = (c >> 1) & 7;
+      v[pp] = aligned_chunk(srow, sw, carry + c * 16, j, delta);
+      if (j == 0) last[pp] = staged_chunk(srow, sw, 7);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const int c = 32 * sw_idx + (4 * half + pp) * 4 + (lane >> 3);
+      uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
+      const int sw = (c >> 1) & 7;
+      *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = v[pp];
+      if (j == 0) *reinterpret_cast<uint4*>(carry + c * 16) = last[pp];
+    }
   }
 }
 
