@@ -343,18 +343,33 @@ def run_gpu(args):
     # Two buffer sets, each larger than the 129 MB L2, alternated step by step.
     sets = [R.build(0), R.build(1)]
 
-    def step(i):
-        R.call(sets[i & 1], stream)
+    def step(i, st=stream):
+        R.call(sets[i & 1], st)
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
 
+    graph = None
+    if args.graph:
+        # Launch-bound small workloads: capture the steps in a CUDA graph so
+        # that host-side launch overhead stays out of the timed region.
+        per_graph = min(args.steps, 100)
+        args.steps = max(1, args.steps // per_graph) * per_graph
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cs = torch.cuda.current_stream()
+            for i in range(per_graph):
+                step(i, cs)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+
     # Timed region: K steps between two events; every 8th step also gets its
-    # own event pair, for the per-launch duration of the kernel.
+    # own event pair, for the per-launch duration of the kernel (graph mode:
+    # the per-step time of the replayed graph).
     every = 8
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(0, args.steps, every)]
+          for _ in range(0, args.steps, every)] if graph is None else []
     t_beg = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     gpu_index = dev.index if ws > 1 else int(
@@ -365,57 +380,71 @@ def run_gpu(args):
     clocks.start()
     time.sleep(0.15)
     t_beg.record(stream)
-    for i in range(args.steps):
-        if i % every == 0:
-            ev[i // every][0].record(stream)
-            step(i)
-            ev[i // every][1].record(stream)
-        else:
-            step(i)
+    if graph is not None:
+        for _ in range(args.steps // per_graph):
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            if i % every == 0:
+                ev[i // every][0].record(stream)
+                step(i)
+                ev[i // every][1].record(stream)
+            else:
+                step(i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clock_info = clocks.stop()
     barrier(ws)
     elapsed = t_beg.elapsed_time(t_end) / 1e3
-    per_launch = [a.elapsed_time(b) / 1e3 for a, b in ev]
+    per_launch = ([a.elapsed_time(b) / 1e3 for a, b in ev] if graph is None
+                  else [elapsed / args.steps])
     max_elapsed = max_over_ranks(elapsed, ws, dev)
     value = whole_job_value(nbytes, args.steps, ws, max_elapsed)
     avg_launch = sum(per_launch) / len(per_launch)
     peak, peak_kind = hbm_peak()
     achieved = nbytes / avg_launch / 1e9
 
-    # End to end through the public API with host buffers: pinned H2D of the
-    # step's inputs, the call, D2H of every output, each step.
+    # End to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory, calls the cast, and copies every
+    # output back to pinned host memory.  Consecutive steps alternate between
+    # two buffer sets on two streams, so that one step's device-to-host copies
+    # overlap the next step's host-to-device copies (separate copy engines).
     e2e = None
     if args.e2e_steps > 0:
-        dev_set = sets[0]
-        host_in = {j: dev_set[j].cpu().pin_memory() for j in R.inputs}
-        host_out = {j: torch.empty(dev_set[j].shape, dtype=dev_set[j].dtype).pin_memory()
-                    for j in R.outputs}
+        streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        host_in = [{j: sets[k][j].cpu().pin_memory() for j in R.inputs} for k in range(2)]
+        host_out = [{j: torch.empty(sets[k][j].shape, dtype=sets[k][j].dtype).pin_memory()
+                     for j in R.outputs} for k in range(2)]
 
-        def e2e_step():
-            for j in R.inputs:
-                dev_set[j].copy_(host_in[j], non_blocking=True)
-            R.call(dev_set, stream)
-            for j in R.outputs:
-                host_out[j].copy_(dev_set[j], non_blocking=True)
+        def e2e_step(i):
+            k = i & 1
+            st = streams[k]
+            with torch.cuda.stream(st):
+                for j in R.inputs:
+                    sets[k][j].copy_(host_in[k][j], non_blocking=True)
+                R.call(sets[k], st)
+                for j in R.outputs:
+                    host_out[k][j].copy_(sets[k][j], non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(ws)
-        a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        b.record(stream)
+        a.record(streams[0])
+        streams[1].wait_event(a)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        streams[0].wait_stream(streams[1])
+        b.record(streams[0])
         torch.cuda.synchronize(dev)
         e_el = max_over_ranks(a.elapsed_time(b) / 1e3, ws, dev)
-        h2d = sum(host_in[j].numel() * host_in[j].element_size() for j in R.inputs)
-        d2h = sum(host_out[j].numel() * host_out[j].element_size() for j in R.outputs)
+        h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
         e2e = {"value": whole_job_value(nbytes, args.e2e_steps, ws, e_el), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": args.e2e_steps, "ms_per_step": 1e3 * e_el / args.e2e_steps}
+               "steps": args.e2e_steps, "ms_per_step": 1e3 * e_el / args.e2e_steps,
+               "pipelining": "2 streams, 2 buffer sets: D2H of step i overlaps H2D of step i+1"}
         del host_in, host_out
 
     cpu = None
@@ -445,7 +474,8 @@ def run_gpu(args):
                          "traffic": measured_traffic() if R.name == "fused" and not args.shape
                          and not args.workload else None,
                          "kernel": R.kernel, "avg_launch_us": 1e6 * avg_launch,
-                         "launch_samples": len(per_launch)},
+                         "launch_samples": len(per_launch),
+                         "timing": "cuda graph replay" if graph is not None else "stream launches"},
             "frac_of_peak": value / ws / peak,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -465,7 +495,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["mx", "reference"], default="mx")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=12)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--shape", type=int, nargs=2, metavar=("M", "K"), default=None,
                    help="fused / dim1: an M x K matrix of the same value mix instead; "
@@ -473,6 +503,8 @@ def main(argv=None):
     p.add_argument("--row", choices=["fused", "dim1", "grouped", "experts", "blocked"],
                    default="fused", help="which row of the hot path one step runs")
     p.add_argument("--workload", default=None, help="named workload for the row")
+    p.add_argument("--graph", action="store_true",
+                   help="replay the timed steps from a CUDA graph (small, launch-bound workloads)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")

@@ -46,11 +46,41 @@ EncodeFn encode_fn() {
   return fn;
 }
 
+// A tensor map depends only on these values, so maps are cached per thread
+// (encoding costs microseconds of host time per call).
+struct MapKey {
+  const void* base;
+  uint64_t inner, outer, stride;
+  uint32_t bin, bout;
+  int dt, l2;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && stride == o.stride &&
+           bin == o.bin && bout == o.bout && dt == o.dt && l2 == o.l2;
+  }
+};
+
+struct MapCache {
+  static constexpr int kEntries = 16;
+  MapKey key[kEntries];
+  CUtensorMap map[kEntries];
+  bool used[kEntries] = {};
+  int next = 0;
+};
+
+thread_local MapCache t_maps;
+
 // 2D tiled map: inner dimension `inner` (elements), `outer` rows `stride`
 // bytes apart, box `bin` x `bout`, 128-byte swizzle.
 int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
               uint64_t outer, uint64_t stride, uint32_t bin, uint32_t bout,
               CUtensorMapL2promotion l2) {
+  const MapKey k = {base, inner, outer, stride, bin, bout, static_cast<int>(dt), static_cast<int>(l2)};
+  for (int i = 0; i < MapCache::kEntries; ++i) {
+    if (t_maps.used[i] && t_maps.key[i] == k) {
+      *m = t_maps.map[i];
+      return MX_OK;
+    }
+  }
   EncodeFn fn = encode_fn();
   if (!fn) return cuda_fail(static_cast<int>(cudaErrorNotSupported));
   const cuuint64_t dims[2] = {inner, outer};
@@ -61,6 +91,11 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(static_cast<int>(cudaErrorInvalidValue));
+  const int slot = t_maps.next;
+  t_maps.next = (slot + 1) % MapCache::kEntries;
+  t_maps.key[slot] = k;
+  t_maps.map[slot] = *m;
+  t_maps.used[slot] = true;
   return MX_OK;
 }
 

@@ -84,45 +84,60 @@ __global__ void __launch_bounds__(1024) group_offsets_kernel(const int32_t* __re
 }
 
 // Scale matrix s (R x C bytes, row-major) -> blocked layout.  One CTA takes
-// one 128-row band and up to 16 column tiles (64 scale columns): it reads the
-// 128 x 64 bytes with coalesced row loads into shared memory, then writes the
-// 16 tiles (8 KB contiguous in the output) as 16-byte chunks.  Storage row i
-// of a tile is rows i, i+32, i+64, i+96, four columns each.  Out-of-range
-// rows / columns are written as zero padding.
+// one 128-row band and up to 32 column tiles (128 scale columns, 16 KB):
+//   - load: 16-byte global loads when C % 16 == 0 and s is 16-byte aligned
+//     (eight lanes per 128-byte row), else byte loads; each lane stores its 16
+//     bytes as four words into shared memory rows of 33 words, so that both
+//     the stores (row r + 4k + m distinct over a warp) and the transposed
+//     reads below hit 32 distinct banks;
+//   - store: the 32 tiles are 16 KB contiguous in the output; lane i of a
+//     warp builds storage row i of one tile (rows i, i+32, i+64, i+96, four
+//     columns each) and writes it with one 16-byte store.
+// Out-of-range rows / columns are written as zero padding.
+constexpr int kBlkCols = 128;                       // scale columns per CTA
+constexpr int kBlkPitch = kBlkCols / 4 + 1;         // words per shared row
+
 __global__ void __launch_bounds__(256) to_blocked_kernel(const uint8_t* __restrict__ s, int64_t R,
                                                         int64_t C, uint8_t* __restrict__ out,
-                                                        int64_t n_ct, int vec4) {
-  __shared__ uint32_t tile[128][17];
+                                                        int64_t n_ct, int vec16) {
+  __shared__ uint32_t tile[128 * kBlkPitch];
   const int64_t rb = blockIdx.y;
-  const int64_t ct0 = static_cast<int64_t>(blockIdx.x) * 16;  // first column tile
+  const int64_t ct0 = static_cast<int64_t>(blockIdx.x) * (kBlkCols / 4);   // first column tile
   const int64_t c0 = ct0 * 4;
-  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-    const int r = i >> 4, wi = i & 15;
+  // 128 rows x 8 chunks of 16 bytes
+  for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
+    const int r = i >> 3, k = i & 7;
     const int64_t row = rb * 128 + r;
-    const int64_t col = c0 + wi * 4;
-    uint32_t v = 0u;
+    const int64_t col = c0 + 16 * k;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (row < R && col < C) {
       const uint8_t* src = s + row * C + col;
-      if (vec4) {
-        v = *reinterpret_cast<const uint32_t*>(src);
+      if (vec16) {
+        v = *reinterpret_cast<const uint4*>(src);
       } else {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          if (col + b < C) v |= static_cast<uint32_t>(src[b]) << (8 * b);
+        for (int b = 0; b < 16; ++b)
+          if (col + b < C) w[b >> 2] |= static_cast<uint32_t>(src[b]) << (8 * (b & 3));
+        v = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    tile[r][wi] = v;
+    uint32_t* dst = tile + r * kBlkPitch + 4 * k;
+    dst[0] = v.x;
+    dst[1] = v.y;
+    dst[2] = v.z;
+    dst[3] = v.w;
   }
   __syncthreads();
-  for (int k = threadIdx.x; k < 16 * 32; k += blockDim.x) {
+  for (int k = threadIdx.x; k < (kBlkCols / 4) * 32; k += blockDim.x) {
     const int j = k >> 5, i = k & 31;
     const int64_t ct = ct0 + j;
     if (ct >= n_ct) break;
     uint4 o;
-    o.x = tile[i][j];
-    o.y = tile[32 + i][j];
-    o.z = tile[64 + i][j];
-    o.w = tile[96 + i][j];
+    o.x = tile[i * kBlkPitch + j];
+    o.y = tile[(32 + i) * kBlkPitch + j];
+    o.z = tile[(64 + i) * kBlkPitch + j];
+    o.w = tile[(96 + i) * kBlkPitch + j];
     *reinterpret_cast<uint4*>(out + (rb * n_ct + ct) * 512 + i * 16) = o;
   }
 }
@@ -140,9 +155,10 @@ int launch_scales_to_blocked(const uint8_t* s, int64_t R, int64_t C, uint8_t* ou
   const int64_t n_ct = (C + 3) / 4;
   const int64_t n_rb = (R + 127) / 128;
   if (n_rb > 65535) return static_cast<int>(cudaErrorInvalidConfiguration);
-  dim3 grid(static_cast<unsigned>((n_ct + 15) / 16), static_cast<unsigned>(n_rb));
-  const int vec4 = (C % 4 == 0) && ((reinterpret_cast<uintptr_t>(s) & 3) == 0);
-  to_blocked_kernel<<<grid, 256, 0, stream>>>(s, R, C, out, n_ct, vec4);
+  dim3 grid(static_cast<unsigned>((n_ct + kBlkCols / 4 - 1) / (kBlkCols / 4)),
+            static_cast<unsigned>(n_rb));
+  const int vec16 = (C % 16 == 0) && ((reinterpret_cast<uintptr_t>(s) & 15) == 0);
+  to_blocked_kernel<<<grid, 256, 0, stream>>>(s, R, C, out, n_ct, vec16);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -359,3 +359,25 @@ def test_3d_expert_workload_sampled():
         assert_bytes_equal(to_np(q1[cols.cuda(), e * N:(e + 1) * N]), oq, "q1 expert %d" % e)
         plain = oracle.from_blocked(to_np(s1[e * per:(e + 1) * per]), K, N // 32)
         assert_bytes_equal(plain[cols.numpy()], os_, "s1 expert %d" % e)
+
+
+def test_cuda_graph_capture_replays_identically():
+    """The C-ABI calls can be captured into a CUDA graph (tensor maps are
+    encoded on the host at capture time) and replay to the same bytes."""
+    x = W.wide(512, 384, 77).cuda()
+    ref = mx.cast_dim0_dim1(x)
+    outs = tuple(torch.empty_like(t) for t in ref)
+    offs = torch.tensor([100, 300, 512], dtype=torch.int32, device="cuda")
+    gref = mx.cast_grouped_m(x, offs)
+    gouts = tuple(torch.empty_like(t) for t in gref)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mx.mx_cast_dim0_dim1(x, *outs)
+        mx.mx_cast_grouped_m(x, offs, *gouts)
+    for t in outs + gouts:
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref + gref, outs + gouts):
+        assert torch.equal(a, b)
