@@ -100,17 +100,19 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 }
 
 // Descriptors for X (M x K bf16) and q1 (K x M bytes, as its even and odd
-// rows).  q1 may be null (not written by TMA in this call).
-int encode_cast_maps(mx::CastMaps* maps, const void* x, int64_t M, int64_t K, const void* q1) {
+// rows, boxes of 128 bytes x q1_rows).  q1 may be null (not written by TMA in
+// this call).
+int encode_cast_maps(mx::CastMaps* maps, const void* x, int64_t M, int64_t K, const void* q1,
+                     unsigned q1_rows = mx::kQ1BoxRowsFused) {
   int rc = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, 128,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
   if (q1) {
-    rc = encode_2d(&maps->q1e, CU_TENSOR_MAP_DATA_TYPE_UINT8, q1, M, K / 2, 2 * M, 128, 64,
+    rc = encode_2d(&maps->q1e, CU_TENSOR_MAP_DATA_TYPE_UINT8, q1, M, K / 2, 2 * M, 128, q1_rows,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (rc) return rc;
     rc = encode_2d(&maps->q1o, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<const uint8_t*>(q1) + M,
-                   M, K / 2, 2 * M, 128, 64, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+                   M, K / 2, 2 * M, 128, q1_rows, CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (rc) return rc;
   } else {
     maps->q1e = maps->x;
@@ -229,7 +231,8 @@ int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, 
   // q1 rows are 16-byte aligned only when M % 16 == 0; then whole tiles may
   // leave by TMA (see the grouped kernel), otherwise all of q1 is written with
   // plain stores.
-  if (int rc = encode_cast_maps(&maps, x, M, K, M % 16 == 0 ? q1 : nullptr)) return rc;
+  if (int rc = encode_cast_maps(&maps, x, M, K, M % 16 == 0 ? q1 : nullptr, mx::kQ1BoxRowsGrouped))
+    return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -69,7 +69,8 @@ constexpr int kMaxSmemGroups = 1024;                         // group table cach
 constexpr int kOffGTab = kOffCarry + kTile * 16;
 constexpr int kGTabBytes = ((2 * kMaxSmemGroups + 1) * 4 + 127) / 128 * 128;
 constexpr int kOffBar = kOffGTab + kGTabBytes;
-constexpr int kNumBars = 2 * kStages + 3 * kStaging;
+constexpr int kNumBars = 2 * kStages + 2 * kStaging;
+constexpr int kQ1GroupBoxRows = static_cast<int>(kQ1BoxRowsGrouped);  // grouped: per-warp q1 box rows
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
@@ -460,7 +461,6 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   uint64_t* empty = bars + kStages;           // [kStages] compute done reading
   uint64_t* sfull = bars + 2 * kStages;       // [kStaging] staging written
   uint64_t* sempty = sfull + kStaging;        // [kStaging] staging drained
-  uint64_t* qdone = sfull + 2 * kStaging;     // [kStaging] grouped: store warps done
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
 
   const int warp = threadIdx.x >> 5;
@@ -501,8 +501,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     }
     for (int o = 0; o < kStaging; ++o) {
       mbar_init(&sfull[o], kComputeWarps);
-      mbar_init(&sempty[o], 1);
-      mbar_init(&qdone[o], store_warps(kMode));
+      mbar_init(&sempty[o], store_warps(kMode));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -540,42 +539,38 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       const Tile T = get_tile<kMode>(p, tab, t);
       uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
-      bool q1_box = kTmaQ1;               // the staged q1 tile leaves as TMA boxes
-      int32_t box_x = T.m0;
       if (kMode == kModeGrouped) {
-        // Grouped: a whole 128-row tile whose q1 rows are 16-byte aligned at
-        // a common offset leaves by TMA, shifted onto the aligned chunks when
-        // that offset is not 0 (which needs the carried chunk of the tile
-        // above and hands its own last chunk to the tile below).  All other
-        // tiles (strip ends, partial tiles, odd M) are stored piecewise.
+        // Grouped: store warp sw owns rows 16*sw .. 16*sw+15 of each q1 half.
+        // A whole 128-row tile whose q1 rows are 16-byte aligned at a common
+        // offset leaves by TMA (one 16-row box per half and warp), shifted
+        // onto the aligned chunks when that offset is not 0 (which needs the
+        // carried chunk of the tile above and hands its own last chunk to the
+        // tile below).  Other tiles (strip ends, partial tiles, odd M) are
+        // stored piecewise.
         const bool cont_prev = (T.cont & 1) && t > first;
         const bool cont_next = (T.cont & 2) && t + 1 < end;
         const int delta = T.m0 & 15;
-        q1_box = p.q1_tma && T.rows == kTile && (delta == 0 || (cont_prev && cont_next));
+        const bool q1_box =
+            p.q1_tma && T.rows == kTile && (delta == 0 || (cont_prev && cont_next));
         if (q1_box) {
           if (delta != 0) shift_q1_rows(q1s, smem + kOffCarry, delta, sw, lane);
-          box_x = T.m0 - delta;
           fence_proxy_async_smem();
+          __syncwarp();
+          const int y = (T.k0 >> 1) + kQ1GroupBoxRows * sw;
+          if (lane == 0 && 2 * static_cast<int64_t>(y) < p.K) {
+            tma_store_2d(&tm_q1e, T.m0 - delta, y, q1s + sw * kQ1GroupBoxRows * 128);
+            tma_store_2d(&tm_q1o, T.m0 - delta, y, q1s + kQ1Half + sw * kQ1GroupBoxRows * 128);
+          }
         } else {
           copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows, cont_prev,
                       cont_next, sw, lane);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qdone[o]);
+      } else if (lane == 0) {
+        tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, q1s);
+        tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, q1s + kQ1Half);
       }
       if (sw == 0) {
-        if (kMode == kModeGrouped) {
-          const bool done = mbar_wait(&qdone[o], ph, abort_flag);
-          if (!__all_sync(0xffffffffu, done)) break;
-        }
-        if (lane == 0) {
-          if (q1_box) {
-            tma_store_2d(&tm_q1e, box_x, T.k0 >> 1, q1s);
-            tma_store_2d(&tm_q1o, box_x, T.k0 >> 1, q1s + kQ1Half);
-          }
-          if (kDim0) bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
-          bulk_commit();
-        }
+        if (lane == 0 && kDim0) bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
         if (T.s1_dst) {
           // dim1 scales are staged as [M-block][column]; storage row `lane` of
           // the blocked tile holds columns lane, lane+32, lane+64, lane+96,
@@ -592,14 +587,15 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
           }
           *reinterpret_cast<uint4*>(T.s1_dst + lane * 16) = w;
         }
-        __syncwarp();
-        if (lane == 0) {
-          bulk_wait_read<0>();
-          mbar_arrive(&sempty[o]);
-        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(&sempty[o]);
       }
     }
-    if (sw == 0 && lane == 0) bulk_wait<0>();
+    if (lane == 0) bulk_wait<0>();
     __syncwarp();
   } else {
     // compute warps

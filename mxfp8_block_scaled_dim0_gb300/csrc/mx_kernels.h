@@ -9,12 +9,16 @@
 namespace mx {
 
 // TMA descriptors of one cast call: x (bf16, two 64-column halves per tile,
-// 128B swizzle) and the even / odd rows of q1 (64 x 128-byte boxes).
+// 128B swizzle) and the even / odd rows of q1 (boxes of 128 bytes x 64 rows,
+// or x 16 rows for the grouped kernel's per-warp stores).
 struct CastMaps {
   CUtensorMap x;
   CUtensorMap q1e;
   CUtensorMap q1o;
 };
+
+constexpr unsigned kQ1BoxRowsFused = 64;
+constexpr unsigned kQ1BoxRowsGrouped = 16;
 
 int smem_bytes_cast();
 int threads_cast();
