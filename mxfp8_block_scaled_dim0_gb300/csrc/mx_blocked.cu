@@ -21,7 +21,7 @@ constexpr int kErrGroups = -5;   // MX_ERR_GROUPS
 //   col_offs[g] = sum_{h<g} ceil(m_h / 128) * 4
 // and status = 0, or MX_ERR_GROUPS if an offset is negative, decreases,
 // exceeds M, or the last one is not M.
-__global__ void __launch_bounds__(1024) group_offsets_kernel(const int32_t* __restrict__ offs,
+__global__ void __launch_bounds__(256) group_offsets_kernel(const int32_t* __restrict__ offs,
                                                             int G, int64_t M,
                                                             int64_t* __restrict__ row_offs,
                                                             int64_t* __restrict__ col_offs,
@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(256) to_blocked_kernel(const uint8_t* __restri
 
 int launch_group_offsets(const int32_t* offs, int G, int64_t M, int64_t* row_offs,
                          int64_t* col_offs, int32_t* status, cudaStream_t stream) {
-  group_offsets_kernel<<<1, 1024, 0, stream>>>(offs, G, M, row_offs, col_offs, status);
+  // 256 threads: small enough (in registers) to share an SM with a CTA of
+  // the cast kernel that follows it as a programmatic dependent.
+  group_offsets_kernel<<<1, 256, 0, stream>>>(offs, G, M, row_offs, col_offs, status);
   return static_cast<int>(cudaGetLastError());
 }
 

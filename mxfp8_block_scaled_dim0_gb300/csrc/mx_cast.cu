@@ -590,9 +590,11 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       }
       __syncwarp();
       if (lane == 0) {
+        // Keep the newest bulk group in flight: the buffer of the previous
+        // tile is released once its own group has been read.
         bulk_commit();
-        bulk_wait_read<0>();
-        mbar_arrive(&sempty[o]);
+        bulk_wait_read<1>();
+        if (it > 0) mbar_arrive(&sempty[static_cast<int>((it - 1) % kStaging)]);
       }
     }
     if (lane == 0) bulk_wait<0>();
