@@ -301,11 +301,13 @@ def make_row(row, args, dev, rank):
     if row == "experts":
         wl = args.workload or "experts16x8192x5120"
         E, N, K = W.WORKLOADS[wl].shape
+        if args.shape:
+            E, N, K = args.shape
+            wl = "custom_experts_%dx%dx%d" % (E, N, K)
         ns = mx.mx_3d_scale_bytes(E, N, K)
 
         def build(i):
-            w = W.make(wl, device=dev)["x"] if i == 0 else \
-                W.experts(E, N, K, W.WORKLOADS[wl].seed + 100 * i, device=dev)
+            w = W.experts(E, N, K, 1005 + 100 * i, device=dev)
             return (w, torch.empty((K, E * N), dtype=torch.uint8, device=dev), u8(ns))
         return Row("experts", wl, "mx_cast_kernel<experts>", 3 * E * N * K + ns, 1, build,
                    lambda a, st: mx.mx_cast_3d_dim1(*a, stream=st), (0,), (1, 2))
@@ -497,9 +499,9 @@ def main(argv=None):
     p.add_argument("--impl", choices=["mx", "reference"], default="mx")
     p.add_argument("--e2e-steps", type=int, default=12)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--shape", type=int, nargs=2, metavar=("M", "K"), default=None,
-                   help="fused / dim1: an M x K matrix of the same value mix instead; "
-                        "blocked: the R x C scale matrix")
+    p.add_argument("--shape", type=int, nargs="+", default=None,
+                   help="fused / dim1: M K of a matrix of the same value mix instead; "
+                        "experts: E N K; blocked: R C of the scale matrix (profiling)")
     p.add_argument("--row", choices=["fused", "dim1", "grouped", "experts", "blocked"],
                    default="fused", help="which row of the hot path one step runs")
     p.add_argument("--workload", default=None, help="named workload for the row")
