@@ -450,7 +450,8 @@ def run_gpu(args):
         del host_in, host_out
 
     cpu = None
-    if rank == 0 and ws == 1 and args.cpu_seconds > 0 and R.name == "fused" and not args.shape:
+    if (rank == 0 and ws == 1 and args.cpu_seconds > 0 and R.name == "fused" and not args.shape
+            and not args.workload):
         gbs, rows, secs = time_oracle(seconds_budget=args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "first %d rows x 16384 cols of the 16384x16384 workload (same value "
