@@ -334,14 +334,25 @@ __device__ __forceinline__ void store_partial(uint8_t* g, const uint4& v, int lo
 // extended chunk j + 1) of the extended row [cslot | staged row].  Two
 // conflict-free 16-byte loads; the uniform word offset (16 - delta) / 4 is
 // applied with three levels of selects, the byte offset with funnel shifts.
-__device__ __forceinline__ uint4 window_q(const uint4& a, const uint4& b, int q, uint32_t r) {
-  // window words q .. q+4 of (a, b, 0...), q uniform; funnel-shifted by r bits
+__device__ __forceinline__ uint4 aligned_chunk(const uint8_t* srow, int sw, const uint8_t* cslot,
+                                               int j, int delta) {
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const uint4 a = j == 0 ? *reinterpret_cast<const uint4*>(cslot)
+                         : *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4));
+  const uint4 b = j <= 7 ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : zero;
+  const int s = 16 - delta;                          // 1 .. 16
+  const int q = s >> 2;                              // word offset 0 .. 4
+  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
+  // w[i] = window word q + i, i = 0..4 (window words 8.. are zero)
   const uint32_t W0 = a.x, W1 = a.y, W2 = a.z, W3 = a.w, W4 = b.x, W5 = b.y, W6 = b.z, W7 = b.w;
   const bool q1b = q & 1, q2b = q & 2, q4b = q & 4;
+  // shift by (q & 1)
   const uint32_t t0 = q1b ? W1 : W0, t1 = q1b ? W2 : W1, t2 = q1b ? W3 : W2, t3 = q1b ? W4 : W3,
                  t4 = q1b ? W5 : W4, t5 = q1b ? W6 : W5, t6 = q1b ? W7 : W6, t7 = q1b ? 0u : W7;
+  // shift by (q & 2)
   const uint32_t u0 = q2b ? t2 : t0, u1 = q2b ? t3 : t1, u2 = q2b ? t4 : t2, u3 = q2b ? t5 : t3,
                  u4 = q2b ? t6 : t4, u5 = q2b ? t7 : t5, u6 = q2b ? 0u : t6, u7 = q2b ? 0u : t7;
+  // shift by (q & 4)
   const uint32_t x0 = q4b ? u4 : u0, x1 = q4b ? u5 : u1, x2 = q4b ? u6 : u2, x3 = q4b ? u7 : u3,
                  x4 = q4b ? 0u : u4;
   uint4 o;
@@ -350,43 +361,6 @@ __device__ __forceinline__ uint4 window_q(const uint4& a, const uint4& b, int q,
   o.z = __funnelshift_r(x2, x3, r);
   o.w = __funnelshift_r(x3, x4, r);
   return o;
-}
-
-// Same window with the word offset Q known at compile time: register picks
-// and four funnel shifts.
-template <int Q>
-__device__ __forceinline__ uint4 window_fixed(const uint4& a, const uint4& b, uint32_t r) {
-  const uint32_t W[9] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, 0u};
-  uint4 o;
-  o.x = __funnelshift_r(W[Q + 0], W[Q + 1], r);
-  o.y = __funnelshift_r(W[Q + 1], W[Q + 2], r);
-  o.z = __funnelshift_r(W[Q + 2], W[Q + 3], r);
-  o.w = __funnelshift_r(W[Q + 3], W[Q + 4], r);
-  return o;
-}
-
-__device__ __forceinline__ uint4 chunk_pair_a(const uint8_t* srow, int sw, const uint8_t* cslot, int j) {
-  return j == 0 ? *reinterpret_cast<const uint4*>(cslot)
-                : *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4));
-}
-__device__ __forceinline__ uint4 chunk_pair_b(const uint8_t* srow, int sw, int j) {
-  return j <= 7 ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : make_uint4(0u, 0u, 0u, 0u);
-}
-
-// Grouped mode, q1 rows.  A tile's q1 row segment (its 128 staged bytes)
-// starts `delta` bytes into a 16-byte chunk of q1 (group starts are not
-// aligned).  Chunk j (0..8) of the segment's aligned chunks holds bytes
-// [16j - delta, 16j - delta + 16) of the segment; bytes before 0 are the
-// previous tile's last bytes.  Those come from `cslot`, which holds the
-// previous tile's raw last 16 bytes (its carried chunk), so chunk j is bytes
-// [16 - delta, 32 - delta) of the 32-byte window (extended chunk j, extended
-// chunk j + 1) of the extended row [cslot | staged row]: two conflict-free
-// 16-byte loads, a word offset (16 - delta) / 4 and a byte funnel shift.
-__device__ __forceinline__ uint4 aligned_chunk(const uint8_t* srow, int sw, const uint8_t* cslot,
-                                               int j, int delta) {
-  const int s = 16 - delta;
-  return window_q(chunk_pair_a(srow, sw, cslot, j), chunk_pair_b(srow, sw, j), s >> 2,
-                  8u * static_cast<uint32_t>(s & 3));
 }
 
 __device__ __forceinline__ uint4 staged_chunk(const uint8_t* srow, int sw, int k) {
@@ -399,65 +373,29 @@ __device__ __forceinline__ uint4 staged_chunk(const uint8_t* srow, int sw, int k
 // 16-byte aligned 128-byte TMA box.  The row's raw last 16 bytes become the
 // carried chunk of the next tile.  Rows 32*sw_idx .. +31, eight lanes per row
 // (lane j takes chunk j); every read happens before any write.
-template <int Q>
-__device__ __forceinline__ void shift_q1_rows_q(uint8_t* q1s, uint8_t* carry, uint32_t r,
-                                                bool cont_next, uint8_t* q1, int64_t M, int64_t K,
-                                                int m0, int k0, int delta, int sw_idx, int lane) {
+__device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta, int sw_idx,
+                                              int lane) {
   const int j = lane & 7;
 #pragma unroll
-  for (int part = 0; part < 4; ++part) {
-    uint4 v[2], last[2];
+  for (int half = 0; half < 2; ++half) {
+    uint4 v[4], last[4];
 #pragma unroll
-    for (int pp = 0; pp < 2; ++pp) {
-      const int c = 32 * sw_idx + (2 * part + pp) * 4 + (lane >> 3);
+    for (int pp = 0; pp < 4; ++pp) {
+      const int c = 32 * sw_idx + (4 * half + pp) * 4 + (lane >> 3);
       const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
       const int sw = (c >> 1) & 7;
-      v[pp] = window_fixed<Q>(chunk_pair_a(srow, sw, carry + c * 16, j), chunk_pair_b(srow, sw, j), r);
+      v[pp] = aligned_chunk(srow, sw, carry + c * 16, j, delta);
       if (j == 0) last[pp] = staged_chunk(srow, sw, 7);
     }
     __syncwarp();
 #pragma unroll
-    for (int pp = 0; pp < 2; ++pp) {
-      const int c = 32 * sw_idx + (2 * part + pp) * 4 + (lane >> 3);
+    for (int pp = 0; pp < 4; ++pp) {
+      const int c = 32 * sw_idx + (4 * half + pp) * 4 + (lane >> 3);
       uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
       const int sw = (c >> 1) & 7;
       *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = v[pp];
-      if (j == 0) {
-        if (cont_next) {
-          *reinterpret_cast<uint4*>(carry + c * 16) = last[pp];
-        } else {
-          // strip end: the segment's last `delta` bytes, stored piecewise
-          const int64_t kk = static_cast<int64_t>(k0) + c;
-          if (kk < K) {
-            const int64_t A = kk * M + m0;
-            store_partial(q1 + (A - delta) + 128, window_fixed<Q>(last[pp], make_uint4(0u, 0u, 0u, 0u), r),
-                          0, delta);
-          }
-        }
-      }
+      if (j == 0) *reinterpret_cast<uint4*>(carry + c * 16) = last[pp];
     }
-  }
-}
-
-// Grouped mode, whole tile of a column strip whose tile above was handled by
-// this CTA: rewrite the staged q1 rows in place onto their aligned chunks
-// (chunk 0 completes the previous tile's partial last chunk from the carried
-// bytes), so that each row is one 16-byte aligned 128-byte TMA box.  The
-// row's raw last 16 bytes become the carried chunk of the tile below, or,
-// at a strip end, its last `delta` bytes are stored piecewise.  Rows 32*sw_idx
-// .. +31, eight lanes per row (lane j takes chunk j); every read of a row
-// happens before any write to it.  The word offset (16 - delta) / 4 is
-// uniform over the tile, so it is dispatched once.
-__device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta,
-                                              bool cont_next, uint8_t* q1, int64_t M, int64_t K,
-                                              int m0, int k0, int sw_idx, int lane) {
-  const int s = 16 - delta;
-  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
-  switch (s >> 2) {
-    case 0: shift_q1_rows_q<0>(q1s, carry, r, cont_next, q1, M, K, m0, k0, delta, sw_idx, lane); break;
-    case 1: shift_q1_rows_q<1>(q1s, carry, r, cont_next, q1, M, K, m0, k0, delta, sw_idx, lane); break;
-    case 2: shift_q1_rows_q<2>(q1s, carry, r, cont_next, q1, M, K, m0, k0, delta, sw_idx, lane); break;
-    default: shift_q1_rows_q<3>(q1s, carry, r, cont_next, q1, M, K, m0, k0, delta, sw_idx, lane); break;
   }
 }
 
@@ -606,17 +544,16 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
         // A whole 128-row tile whose q1 rows are 16-byte aligned at a common
         // offset leaves by TMA (one 16-row box per half and warp), shifted
         // onto the aligned chunks when that offset is not 0 (which needs the
-        // carried chunk of the tile above; its own last chunk goes to the
-        // tile below, or is stored piecewise at a strip end).  Other tiles
-        // (strip starts, partial tiles, odd M) are stored piecewise.
+        // carried chunk of the tile above and hands its own last chunk to the
+        // tile below).  Other tiles (strip ends, partial tiles, odd M) are
+        // stored piecewise.
         const bool cont_prev = (T.cont & 1) && t > first;
         const bool cont_next = (T.cont & 2) && t + 1 < end;
         const int delta = T.m0 & 15;
-        const bool q1_box = p.q1_tma && T.rows == kTile && (delta == 0 || cont_prev);
+        const bool q1_box =
+            p.q1_tma && T.rows == kTile && (delta == 0 || (cont_prev && cont_next));
         if (q1_box) {
-          if (delta != 0)
-            shift_q1_rows(q1s, smem + kOffCarry, delta, cont_next, p.q1, p.M, p.K, T.m0, T.k0, sw,
-                          lane);
+          if (delta != 0) shift_q1_rows(q1s, smem + kOffCarry, delta, sw, lane);
           fence_proxy_async_smem();
           __syncwarp();
           const int y = (T.k0 >> 1) + kQ1GroupBoxRows * sw;
