@@ -145,6 +145,13 @@ int mx_last_cuda_error(void);
  * current device, clearing it if `clear` is non-zero, or MX_ERR_CUDA. */
 int mx_watchdog(int clear);
 
+/* Diagnostic: enqueue one warp that waits, with a limit of `wait_ns`
+ * nanoseconds (1e3 .. 1e10), on a barrier that nothing completes.  The wait
+ * gives up, sets the watchdog word read by mx_watchdog() and the kernel
+ * returns normally: the failure path of the bounded waits, exercised without
+ * any fault.  Returns MX_OK, MX_ERR_SHAPE or MX_ERR_CUDA. */
+int mx_selftest_watchdog(int64_t wait_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

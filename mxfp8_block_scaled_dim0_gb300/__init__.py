@@ -30,7 +30,7 @@ MX_ERR_GROUPS = -5
 ABI_SYMBOLS = (
     "mx_cast_dim0_dim1", "mx_cast_dim1", "mx_scales_to_blocked", "mx_cast_grouped_m",
     "mx_cast_3d_dim1", "mx_blocked_bytes", "mx_grouped_m_scale_bytes", "mx_3d_scale_bytes",
-    "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
+    "mx_strerror", "mx_last_cuda_error", "mx_watchdog", "mx_selftest_watchdog",
 )
 
 
@@ -68,6 +68,7 @@ def _lib():
             "mx_strerror": ([ctypes.c_int], ctypes.c_char_p),
             "mx_last_cuda_error": ([], ctypes.c_int),
             "mx_watchdog": ([ctypes.c_int], ctypes.c_int),
+            "mx_selftest_watchdog": ([I64, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -186,6 +187,12 @@ def mx_cast_3d_dim1(w, q1, s1_blk, stream=None):
     _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), 1)
     _check(_lib().mx_cast_3d_dim1(_ptr(w), E, N, K, _ptr(q1), _ptr(s1_blk), _stream(stream)),
            "mx_cast_3d_dim1")
+
+
+def mx_selftest_watchdog(wait_ns=50_000_000, stream=None):
+    """Run the bounded-wait failure path on the device (no fault): a warp
+    waits on a barrier that never completes and gives up after wait_ns."""
+    _check(_lib().mx_selftest_watchdog(int(wait_ns), _stream(stream)), "mx_selftest_watchdog")
 
 
 def mx_watchdog(clear=True):

@@ -179,6 +179,12 @@ int mx_watchdog(int clear) {
   return v;
 }
 
+int mx_selftest_watchdog(int64_t wait_ns, void* stream) {
+  if (wait_ns < 1000 || wait_ns > int64_t{10} * 1000 * 1000 * 1000) return MX_ERR_SHAPE;
+  return launch_rc(mx::launch_watchdog_selftest(static_cast<uint64_t>(wait_ns),
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, void* q1,
                       void* s1_blk, void* stream) {
   if (!x || !q0 || !s0_blk || !q1 || !s1_blk) return MX_ERR_NULL;

@@ -774,6 +774,28 @@ int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_
   return launch<kModeGrouped>(maps, prm, grid, stream);
 }
 
+// Watchdog self-test: one warp waits on an mbarrier that nothing arrives at,
+// with a short limit.  The wait must give up, set the device watchdog word and
+// let the kernel return normally (no trap, no fault, context stays usable).
+__global__ void __launch_bounds__(32) watchdog_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0u, &abort_flag, limit_ns);
+  __syncwarp();
+  if (threadIdx.x == 0 && !ok) atomicOr(&g_watchdog, 1);
+}
+
+int launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t stream) {
+  watchdog_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return static_cast<int>(cudaGetLastError());
+}
+
 int read_watchdog(int* out, bool clear) {
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_watchdog, sizeof(int));

@@ -109,3 +109,8 @@ def test_product_path_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"\b(import|from)\s+oracle\b|mx_oracle|oracle_\w+\(", text), f
+
+
+def test_selftest_watchdog_rejects_bad_limits(lib):
+    assert lib.mx_selftest_watchdog(0, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_selftest_watchdog(10**11, None) == mx.MX_ERR_SHAPE
