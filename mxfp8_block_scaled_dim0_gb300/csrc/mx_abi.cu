@@ -242,10 +242,8 @@ int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, 
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (int rc = mx::launch_group_offsets(offs, G, M, s0_row_offs, s1_col_offs, status, st))
-    return cuda_fail(rc);
   return launch_rc(mx::launch_cast_grouped(maps, M, K, offs, G, q0, q1, s0_blk, s0_row_offs,
-                                           s1_blk, status, sms, st));
+                                           s1_col_offs, s1_blk, status, sms, st));
 }
 
 int mx_cast_3d_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q1, void* s1_blk,

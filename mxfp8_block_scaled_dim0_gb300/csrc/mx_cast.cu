@@ -65,14 +65,15 @@ constexpr int kOffQ1 = kOffIn + kStages * kInBytes;
 constexpr int kOffS0 = kOffQ1 + kStaging * kQBytes;
 constexpr int kOffS1 = kOffS0 + kStaging * kScaleTile;
 constexpr int kOffCarry = kOffS1 + kStaging * kScaleTile;   // grouped: 128 x 16 B
-constexpr int kMaxSmemGroups = 1024;                         // group table cached in smem
+// group table in smem up to kMaxSmemGroups groups (mx_kernels.h)
 constexpr int kOffGTab = kOffCarry + kTile * 16;
 constexpr int kGTabBytes = ((2 * kMaxSmemGroups + 1) * 4 + 127) / 128 * 128;
 constexpr int kOffBar = kOffGTab + kGTabBytes;
 constexpr int kNumBars = 2 * kStages + 2 * kStaging;
 constexpr int kQ1GroupBoxRows = static_cast<int>(kQ1BoxRowsGrouped);  // grouped: per-warp q1 box rows
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
-constexpr int kSmemUsed = kOffFlag + 16;
+constexpr int kSmemUsed = kOffFlag + 16;   // flag: abort (+0), bad group offsets (+4)
+constexpr int kStatusBadGroups = -5;        // MX_ERR_GROUPS
 constexpr int kSmemBytes = kSmemUsed + 1024;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -113,8 +114,11 @@ struct Params {
   int32_t nb4;              // ceil4(N / 32)
   // grouped
   const int32_t* offs;
-  const int64_t* row_offs;  // s0_row_offs (G + 1)
+  const int64_t* row_offs;  // s0_row_offs (G + 1), from group_offsets_kernel (G > kMaxSmemGroups)
   const int32_t* status;
+  int64_t* row_offs_out;    // G <= kMaxSmemGroups: written by CTA 0 of this kernel
+  int64_t* col_offs_out;
+  int32_t* status_out;
   int32_t G;
   int32_t k128;             // ceil128(K)
   int32_t q1_tma;           // grouped: q1 rows 16-byte aligned (M % 16 == 0), so
@@ -137,9 +141,7 @@ struct GroupTab {
   }
 };
 
-__device__ __forceinline__ int64_t grouped_tiles(const Params& p) {
-  return (p.row_offs[p.G] >> 7) * p.n_kt;
-}
+
 
 // Tile t of the launch.  2D / 3D modes: row-major over (M tiles, K tiles).
 // Grouped mode: ordered by group, then K tile, then M tile within the group,
@@ -469,25 +471,72 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   GroupTab tab = {nullptr, nullptr, p.row_offs, p.offs};
   int64_t first, end, step;
   if (kMode == kModeGrouped) {
-    // The offsets come from the preceding group_offsets_kernel, launched as
-    // this kernel's programmatic prerequisite: wait for it before reading.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (*p.status != 0) return;               // invalid group offsets: write nothing
-    const int64_t n_tiles = grouped_tiles(p);
+    int64_t total_tr;                         // padded tile-rows of all groups
+    if (p.G <= kMaxSmemGroups) {
+      // Up to kMaxSmemGroups groups every CTA builds the group table itself
+      // from the offsets (no separate offsets kernel on the critical path):
+      // validate, count ceil(m_g / 128) tile-rows per group and scan them.
+      // CTA 0 also writes the padded-offset outputs and the status word.
+      int32_t* tr_s = reinterpret_cast<int32_t*>(smem + kOffGTab);
+      int32_t* ends_s = tr_s + kMaxSmemGroups + 1;
+      volatile int* bad_s = reinterpret_cast<volatile int*>(smem + kOffFlag + 4);
+      for (int g = threadIdx.x; g < p.G; g += blockDim.x) ends_s[g] = p.offs[g];
+      __syncthreads();
+      if (warp == 0) {
+        int64_t carry = 0;
+        bool bad = false;
+        for (int base = 0; base < p.G; base += 32) {
+          const int g = base + lane;
+          int64_t tiles = 0;
+          if (g < p.G) {
+            const int64_t hi = ends_s[g];
+            const int64_t lo = g ? static_cast<int64_t>(ends_s[g - 1]) : 0;
+            const bool b = hi < lo || hi < 0 || hi > p.M || (g == p.G - 1 && hi != p.M);
+            bad = bad || b;
+            tiles = b ? 0 : (hi - lo + 127) >> 7;
+          }
+          int64_t incl = tiles;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const int64_t n = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += n;
+          }
+          if (g < p.G) tr_s[g + 1] = static_cast<int32_t>(carry + incl);
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+          tr_s[0] = 0;
+          *bad_s = bad ? 1 : 0;
+        }
+      }
+      __syncthreads();
+      if (*bad_s) {                           // invalid group offsets: write nothing
+        if (blockIdx.x == 0 && threadIdx.x == 0) *p.status_out = kStatusBadGroups;
+        return;
+      }
+      if (blockIdx.x == 0) {
+        for (int g = threadIdx.x; g <= p.G; g += blockDim.x) {
+          p.row_offs_out[g] = static_cast<int64_t>(tr_s[g]) * 128;
+          p.col_offs_out[g] = static_cast<int64_t>(tr_s[g]) * 4;
+        }
+        if (threadIdx.x == 0) *p.status_out = 0;
+      }
+      tab.tr_s = tr_s;
+      tab.ends_s = ends_s;
+      total_tr = tr_s[p.G];
+    } else {
+      // The offsets come from the preceding group_offsets_kernel, launched
+      // as this kernel's programmatic prerequisite: wait for it first.
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (*p.status != 0) return;             // invalid group offsets: write nothing
+      total_tr = p.row_offs[p.G] >> 7;
+    }
+    const int64_t n_tiles = total_tr * p.n_kt;
     // contiguous, balanced runs of tiles per CTA
     first = n_tiles * blockIdx.x / gridDim.x;
     end = n_tiles * (blockIdx.x + 1) / gridDim.x;
     step = 1;
-    if (p.G <= kMaxSmemGroups) {
-      int32_t* tr_s = reinterpret_cast<int32_t*>(smem + kOffGTab);
-      int32_t* ends_s = tr_s + kMaxSmemGroups + 1;
-      for (int g = threadIdx.x; g <= p.G; g += blockDim.x) {
-        tr_s[g] = static_cast<int32_t>(p.row_offs[g] >> 7);
-        if (g < p.G) ends_s[g] = p.offs[g];
-      }
-      tab.tr_s = tr_s;
-      tab.ends_s = ends_s;
-    }
   } else {
     first = blockIdx.x;
     end = p.n_tiles;
@@ -656,9 +705,9 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     if (kMode == kModeGrouped) {
       // Zero the scale buffers' tails beyond the last group's padded end.
       const int64_t kb4 = static_cast<int64_t>(p.n_kt) * 4;
-      const int64_t s0_beg = p.row_offs[p.G] * kb4;
+      const int64_t s0_beg = tab.tr(p.G) * 128 * kb4;
       const int64_t s0_end = (p.M + 128 * static_cast<int64_t>(p.G)) * kb4;
-      const int64_t s1_beg = static_cast<int64_t>(p.k128) * (p.row_offs[p.G] >> 5);
+      const int64_t s1_beg = static_cast<int64_t>(p.k128) * (tab.tr(p.G) * 4);
       const int64_t s1_end = static_cast<int64_t>(p.k128) * (((p.M + 31) >> 5) + 4 * p.G);
       const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kComputeThreads + threadIdx.x;
       const int64_t gstride = static_cast<int64_t>(gridDim.x) * kComputeThreads;
@@ -689,7 +738,7 @@ template <int kMode>
 int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t stream) {
   static int attr_rc = set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>));
   if (attr_rc != 0) return attr_rc;
-  if (kMode == kModeGrouped) {
+  if (kMode == kModeGrouped && prm.G > kMaxSmemGroups) {
     // Programmatic dependent launch: the CTAs may start (barrier set-up) while
     // group_offsets_kernel finishes; they wait for it before reading offsets.
     cudaLaunchConfig_t cfg = {};
@@ -752,8 +801,8 @@ int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, v
 }
 
 int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_t* offs, int G,
-                        void* q0, void* q1, void* s0, const int64_t* row_offs, void* s1,
-                        const int32_t* status, int num_sms, cudaStream_t stream) {
+                        void* q0, void* q1, void* s0, int64_t* row_offs, int64_t* col_offs,
+                        void* s1, int32_t* status, int num_sms, cudaStream_t stream) {
   Params prm = {};
   prm.q0 = static_cast<uint8_t*>(q0);
   prm.M = M;
@@ -766,9 +815,16 @@ int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_
   prm.offs = offs;
   prm.row_offs = row_offs;
   prm.status = status;
+  prm.row_offs_out = row_offs;
+  prm.col_offs_out = col_offs;
+  prm.status_out = status;
   prm.G = G;
   prm.k128 = static_cast<int32_t>((K + 127) / 128 * 128);
   prm.q1_tma = (M % 16) == 0;
+  if (G > kMaxSmemGroups) {
+    // Large group counts: the padded offsets come from a separate kernel.
+    if (int rc = launch_group_offsets(offs, G, M, row_offs, col_offs, status, stream)) return rc;
+  }
   const int64_t bound = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
   const int grid = static_cast<int>(bound < num_sms ? (bound > 0 ? bound : 1) : num_sms);
   return launch<kModeGrouped>(maps, prm, grid, stream);

@@ -29,9 +29,13 @@ int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s
                    int num_sms, cudaStream_t stream);
 int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* s1,
                         int num_sms, cudaStream_t stream);
+// G <= kMaxSmemGroups: one kernel builds the group table itself; larger G:
+// group_offsets_kernel first, then the cast kernel as its programmatic
+// dependent.
+constexpr int kMaxSmemGroups = 1024;
 int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_t* offs, int G,
-                        void* q0, void* q1, void* s0, const int64_t* row_offs, void* s1,
-                        const int32_t* status, int num_sms, cudaStream_t stream);
+                        void* q0, void* q1, void* s0, int64_t* row_offs, int64_t* col_offs,
+                        void* s1, int32_t* status, int num_sms, cudaStream_t stream);
 int launch_group_offsets(const int32_t* offs, int G, int64_t M, int64_t* row_offs,
                          int64_t* col_offs, int32_t* status, cudaStream_t stream);
 int launch_scales_to_blocked(const uint8_t* s, int64_t R, int64_t C, uint8_t* out,

@@ -309,6 +309,24 @@ def test_grouped_multi_tile_runs(M, K, G, seed):
     compare_grouped(W.wide(M, K, seed, zero_frac=0.005), offs)
 
 
+def test_grouped_many_groups_two_kernel_path():
+    """More groups than the cast kernel tabulates itself (1024): the padded
+    offsets come from the separate offsets kernel, launched before it."""
+    M, K = 3000, 64
+    offs = W.group_ends(M, 1500, 91, min_size=0).tolist()
+    compare_grouped(W.wide(M, K, 92, zero_frac=0.01), offs)
+
+
+def test_grouped_many_groups_invalid_offsets():
+    M, K = 3000, 64
+    offs = W.group_ends(M, 1500, 93, min_size=0).tolist()
+    offs[700], offs[701] = offs[701] + 1, offs[700]      # decreasing
+    got = run_grouped(W.normal((M, K), 4), offs, fill=CANARY)
+    assert got["status"] == mx.MX_ERR_GROUPS
+    for k in ("q0", "q1", "s0", "s1"):
+        assert np.all(got[k] == CANARY), k
+
+
 def test_grouped_moe_workload_full():
     """The 16640 x 5120, 4-group MoE workload, every byte."""
     w = W.make("moe16640x5120_g4")
