@@ -468,6 +468,13 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // Programmatic dependent launch: let the next launch in the stream start
+  // its set-up now (it cannot share an SM with this CTA, so it only takes SMs
+  // this grid has left), and wait for every earlier grid to finish, with its
+  // memory visible, before touching any input or output.
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   GroupTab tab = {nullptr, nullptr, p.row_offs, p.offs};
   int64_t first, end, step;
   if (kMode == kModeGrouped) {
@@ -526,9 +533,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       tab.ends_s = ends_s;
       total_tr = tr_s[p.G];
     } else {
-      // The offsets come from the preceding group_offsets_kernel, launched
-      // as this kernel's programmatic prerequisite: wait for it first.
-      asm volatile("griddepcontrol.wait;" ::: "memory");
+      // The offsets come from the preceding group_offsets_kernel (waited for
+      // above, like every earlier grid).
       if (*p.status != 0) return;             // invalid group offsets: write nothing
       total_tr = p.row_offs[p.G] >> 7;
     }
@@ -738,25 +744,22 @@ template <int kMode>
 int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t stream) {
   static int attr_rc = set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>));
   if (attr_rc != 0) return attr_rc;
-  if (kMode == kModeGrouped && prm.G > kMaxSmemGroups) {
-    // Programmatic dependent launch: the CTAs may start (barrier set-up) while
-    // group_offsets_kernel finishes; they wait for it before reading offsets.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(threads_of(kMode));
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return static_cast<int>(cudaLaunchKernelEx(&cfg, mx_cast_kernel<kMode>, maps.x, maps.q1e,
-                                               maps.q1o, prm));
-  }
-  mx_cast_kernel<kMode><<<grid, threads_of(kMode), kSmemBytes, stream>>>(maps.x, maps.q1e, maps.q1o,
-                                                                          prm);
-  return static_cast<int>(cudaGetLastError());
+  // Launched as a programmatic dependent of the previous work in the stream:
+  // when that is a cast kernel (which triggers its dependents early), this
+  // grid's launch and set-up overlap its tail; the kernel waits for it to
+  // complete before any memory access (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads_of(kMode));
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, mx_cast_kernel<kMode>, maps.x, maps.q1e, maps.q1o,
+                                             prm));
 }
 
 }  // namespace
