@@ -59,6 +59,12 @@ def _load():
         lib.oracle_cast_grouped_m.restype = ctypes.c_int
         lib.oracle_cast_3d_dim1.argtypes = [P, I64, I64, I64, P, P]
         lib.oracle_cast_3d_dim1.restype = ctypes.c_int
+        lib.oracle_cast_3d_dim0.argtypes = [P, I64, I64, I64, P, P]
+        lib.oracle_cast_3d_dim0.restype = ctypes.c_int
+        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_dequant_blocked.argtypes = [P, I64, I64, P, P]
+        lib.oracle_dequant_blocked.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -211,6 +217,45 @@ def cast_3d_dim1(w):
     return q1, s1
 
 
+def cast_3d_dim0(w):
+    """(E, N, K) bf16 bits -> q0 (E, N, K) bytes and E per-expert blocked
+    scale tiles concatenated (E * blk(N, K/32) bytes)."""
+    w = _bits(w)
+    E, N, K = w.shape
+    q0 = np.empty((E, N, K), np.uint8)
+    s0 = np.empty(E * blocked_bytes(N, K // 32), np.uint8)
+    rc = _load().oracle_cast_3d_dim0(_ptr(w), E, N, K, _ptr(q0), _ptr(s0))
+    if rc != 0:
+        raise MemoryError("oracle scratch allocation failed")
+    return q0, s0
+
+
+def cast_3d_dim0_dim1(w):
+    """Both directions of a 3D weight: (q0, s0_blk) of cast_3d_dim0 and
+    (q1, s1_blk) of cast_3d_dim1."""
+    return cast_3d_dim0(w) + cast_3d_dim1(w)
+
+
+# ---- dequantisation ---------------------------------------------------------
+
+def double_to_bf16(v: float) -> int:
+    return int(_load().oracle_double_to_bf16(float(v)))
+
+
+def dequant_blocked(q, s_blk):
+    """q (R, C) e4m3 bytes with blocked scales blk(R, C/32) -> (R, C) bf16
+    bits: element value times 2^(scale - 127), rounded once to bf16."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    R, C = q.shape
+    s_blk = np.ascontiguousarray(s_blk, dtype=np.uint8).reshape(-1)
+    if C % 32 or s_blk.size < blocked_bytes(R, C // 32):
+        raise ValueError("C must be a multiple of 32 and s_blk hold blk(R, C/32) bytes")
+    out = np.empty((R, C), np.uint16)
+    if _load().oracle_dequant_blocked(_ptr(q), R, C, _ptr(s_blk), _ptr(out)) != 0:
+        raise MemoryError("oracle scratch allocation failed")
+    return out
+
+
 def library_path() -> str:
     return _build.build()
 
@@ -219,5 +264,6 @@ __all__ = [
     "bf16_to_double", "e4m3_rne_sat", "e4m3_rne_sat_array", "e4m3_to_double", "block_scale",
     "cast_dim0", "cast_dim1", "blocked_bytes", "to_blocked", "from_blocked",
     "cast_dim0_dim1_blocked", "grouped_m_scale_bytes", "cast_grouped_m",
-    "cast_3d_dim1", "library_path",
+    "cast_3d_dim1", "cast_3d_dim0", "cast_3d_dim0_dim1", "double_to_bf16",
+    "dequant_blocked", "library_path",
 ]

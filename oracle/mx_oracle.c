@@ -21,7 +21,9 @@
  * pytorch/ao PR #1869 "triton kernel to cast to mx across dim0 and dim1",
  * summary.  The per-group and per-expert variants follow pytorch/ao PR #2990
  * "[mxfp8 moe training] add compile support" (sync-free padding bound
- * rows + groups*128; 3D weights cast through a reshape to 2D).
+ * rows + groups*128; 3D weights cast through a reshape to 2D).  The inverse,
+ * dequantisation, takes the value of an MX element as its scale times its
+ * element value (OCP MX v1.0) and rounds that product once to bf16.
  *
  * Readings taken where the pages are silent (each is repeated in the design
  * notes):
@@ -375,7 +377,29 @@ int oracle_cast_3d_dim1(const uint16_t *w, int64_t E, int64_t N, int64_t K,
     return 0;
 }
 
-/* ---- dequantisation (used by the error-bound pin) ----------------------- */
+/* ---- 3D expert weights, dim0 per expert -------------------------------- */
+
+/* w is (E, N, K) bf16, read as the 2D matrix (E*N, K).  q0 is its dim0 copy,
+ * (E*N) x K bytes in the same order as w.  Expert e's scales are rows
+ * [e*N, (e+1)*N) of the dim0 scale matrix, an (N, K/32) block that is put in
+ * blocked layout on its own at byte e * blk(N, K/32).  K % 32 == 0; N >= 1
+ * need not be a multiple of 32 (dim0 blocks run along K). */
+int oracle_cast_3d_dim0(const uint16_t *w, int64_t E, int64_t N, int64_t K,
+                        uint8_t *q0, uint8_t *s0_blk)
+{
+    int64_t M = E * N, Kb = K / 32;
+    int64_t per = oracle_blocked_bytes(N, Kb);
+    uint8_t *s0 = malloc((size_t)(M * Kb) + 1);
+    if (!s0)
+        return -1;
+    oracle_cast_dim0(w, M, K, q0, s0);
+    for (int64_t e = 0; e < E; e++)
+        oracle_to_blocked(s0 + e * N * Kb, N, Kb, s0_blk + e * per);
+    free(s0);
+    return 0;
+}
+
+/* ---- dequantisation --------------------------------------------------- */
 
 /* Exact value of an e4m3fn byte (NaN for 0x7F / 0xFF). */
 double oracle_e4m3_to_double(uint8_t b)
@@ -391,4 +415,63 @@ double oracle_e4m3_to_double(uint8_t b)
     else
         mag = ldexp((double)(8 + man), ex - 7 - 3);
     return sign ? -mag : mag;
+}
+
+/* bf16 bit pattern nearest to v: round to nearest, ties to even, over the
+ * whole bf16 range (subnormals m * 2^-133 kept; a magnitude that rounds to
+ * 2^128 or beyond becomes infinity, as in IEEE 754 rounding).  NaN -> 0x7FC0. */
+uint16_t oracle_double_to_bf16(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0x0000;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80;
+    int p;
+    frexp(a, &p);                       /* a in [2^(p-1), 2^p) */
+    int e = p - 1;
+    if (e < -126)
+        e = -126;                       /* subnormal range: fixed spacing 2^-133 */
+    double spacing = ldexp(1.0, e - 7); /* 7 fraction bits */
+    double r = nearbyint(a / spacing) * spacing;
+    if (r >= ldexp(1.0, 128))
+        return sign | 0x7F80;
+    if (r < ldexp(1.0, -126))           /* subnormal (or zero) */
+        return sign | (uint16_t)(r / ldexp(1.0, -133));
+    double f = frexp(r, &p);            /* r = (2f) * 2^(p-1) */
+    int ex = p - 1;
+    int mant = (int)((2.0 * f - 1.0) * 128.0);
+    return sign | (uint16_t)(((ex + 127) << 7) | mant);
+}
+
+/* MX dequantisation of one matrix: q (R x C e4m3 bytes, blocks of 32 along
+ * rows, C % 32 == 0) and its scales in blocked layout (blk(R, C/32) bytes) ->
+ * bf16 bits out[r][c] = bf16(e4m3(q[r][c]) * 2^(s - 127)), where s is the
+ * scale byte of (r, c / 32).  The value of an MX element is the product of
+ * its scale and its element value (OCP MX v1.0); the product is exact in
+ * double and rounded once to bf16.  A NaN scale (0xFF) or NaN element gives
+ * NaN (0x7FC0).  Returns 0, or -1 if scratch memory could not be had. */
+int oracle_dequant_blocked(const uint8_t *q, int64_t R, int64_t C, const uint8_t *s_blk,
+                           uint16_t *out)
+{
+    int64_t Cb = C / MX_BLOCK;
+    uint8_t *s = malloc((size_t)(R * Cb) + 1);
+    if (!s)
+        return -1;
+    oracle_from_blocked(s_blk, R, Cb, s);
+    for (int64_t r = 0; r < R; r++) {
+        for (int64_t c = 0; c < C; c++) {
+            uint8_t sc = s[r * Cb + c / MX_BLOCK];
+            double v = oracle_e4m3_to_double(q[r * C + c]);
+            if (sc == 0xFF || isnan(v))
+                out[r * C + c] = 0x7FC0;
+            else
+                out[r * C + c] = oracle_double_to_bf16(ldexp(v, (int)sc - E8M0_BIAS));
+        }
+    }
+    free(s);
+    return 0;
 }

@@ -344,3 +344,123 @@ def test_3d_reductions():
     q1a, s1a = oracle.cast_3d_dim1(w[:1])
     pq, ps = oracle.cast_dim1(w[0])
     assert np.array_equal(q1a, pq) and np.array_equal(s1a, oracle.to_blocked(ps))
+
+
+def test_3d_dim0_reductions():
+    """cast_3d_dim0 is the dim0 cast of the (E*N, K) view with each expert's
+    scale rows blocked on their own: per-expert 2D casts give the same bytes,
+    and with N % 128 == 0 the layout equals blocking the whole scale matrix."""
+    for E, N, K in [(3, 50, 96), (2, 96, 160), (2, 128, 64), (1, 1, 32)]:
+        w = W.bf16_bits(W.experts(E, N, K, 23))
+        q0, s0 = oracle.cast_3d_dim0(w)
+        per = oracle.blocked_bytes(N, K // 32)
+        assert s0.size == E * per
+        for e in range(E):
+            pq, ps = oracle.cast_dim0(w[e])
+            assert np.array_equal(q0[e], pq)
+            assert np.array_equal(s0[e * per:(e + 1) * per], oracle.to_blocked(ps))
+        if N % 128 == 0:
+            q2, s2 = oracle.cast_dim0(w.reshape(E * N, K))
+            assert np.array_equal(s0, oracle.to_blocked(s2))
+    w = W.bf16_bits(W.experts(2, 64, 96, 29))
+    q0, s0, q1, s1 = oracle.cast_3d_dim0_dim1(w)
+    assert np.array_equal(q1, oracle.cast_3d_dim1(w)[0])
+    assert np.array_equal(q0, oracle.cast_3d_dim0(w)[0])
+
+
+# ---- dequantisation ----------------------------------------------------------
+
+def _golden_dequant():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "hand_worked_dequant.txt")
+    cases = []
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, q, s, out = [t.strip() for t in line.split("|")]
+        cases.append((name, int(q, 16), int(s, 16), None if out == "nan" else int(out, 16)))
+    return cases
+
+
+def _dequant_pairs(qs, ss):
+    """Dequantise element bytes qs with scale bytes ss (one scale per 32-element
+    row block): lay the pairs out as rows of 32 copies."""
+    n = len(qs)
+    q = np.repeat(np.asarray(qs, np.uint8)[:, None], 32, axis=1)
+    s_plain = np.asarray(ss, np.uint8).reshape(n, 1)
+    out = oracle.dequant_blocked(q, oracle.to_blocked(s_plain))
+    assert np.all(out == out[:, :1])
+    return out[:, 0]
+
+
+def test_dequant_hand_worked():
+    cases = _golden_dequant()
+    assert len(cases) >= 20
+    got = _dequant_pairs([c[1] for c in cases], [c[2] for c in cases])
+    for (name, _, _, want), g in zip(cases, got):
+        if want is None:
+            assert (g & 0x7F80) == 0x7F80 and (g & 0x7F), name
+        else:
+            assert g == want, (name, hex(g), hex(want))
+
+
+def _bf16_rne_bits(f32):
+    """Independent float32 -> bf16 rounding (nearest, ties to even) by integer
+    arithmetic on the bit pattern; callers pass finite or infinite values."""
+    u = np.asarray(f32, np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def test_dequant_every_element_every_scale():
+    """All 256 x 255 (element, finite scale) pairs against the product taken in
+    float32 (exact here: 4 significant bits, exponents down to 2^-136) and
+    rounded to bf16 by bit arithmetic; NaN elements give NaN."""
+    qv = np.arange(256, dtype=np.uint8).view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+    qs = np.tile(np.arange(256, dtype=np.uint8), 255)
+    ss = np.repeat(np.arange(255, dtype=np.uint8), 256)
+    got = _dequant_pairs(qs, ss)
+    prod = qv[qs] * np.exp2(ss.astype(np.float64) - 127.0)
+    nan = np.isnan(prod)
+    with np.errstate(over="ignore"):
+        want = _bf16_rne_bits(prod[~nan].astype(np.float32))
+    assert np.array_equal(got[~nan], want)
+    assert np.all(((got[nan] & 0x7F80) == 0x7F80) & ((got[nan] & 0x7F) != 0))
+
+
+def test_dequant_round_trip_exact_blocks():
+    """A block of e4m3 values times 2^j whose largest magnitude lies in
+    [256, 448] quantises with scale 127 + j and no rounding, so dequantising
+    gives the input back exactly (also through the dim1 direction)."""
+    rng = np.random.default_rng(31)
+    grid = np.arange(256, dtype=np.uint8).view(ml_dtypes.float8_e4m3fn).astype(np.float64)
+    grid = grid[np.isfinite(grid)]
+    M, K = 64, 128
+    v = rng.choice(grid, size=(M, K))
+    v.reshape(M, K // 32, 32)[:, :, 0] = rng.choice([256.0, 288.0, 448.0, -320.0], size=(M, K // 32))
+    j = rng.integers(-100, 100, size=(M, K // 32, 1))
+    x = (v.reshape(M, K // 32, 32) * np.exp2(j.astype(np.float64))).reshape(M, K)
+    bits = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(np_bf16_values(bits), x)
+    q0, s0, q1, s1 = oracle.cast_dim0_dim1_blocked(bits)
+    assert np.array_equal(oracle.from_blocked(s0, M, K // 32), (127 + j[:, :, 0]).astype(np.uint8))
+    assert np.array_equal(oracle.dequant_blocked(q0, s0), bits)
+
+
+def test_dequant_of_cast_is_within_half_ulp():
+    """dequant(cast(x)) differs from x by at most half an e4m3 step at the
+    block's scale, except saturated elements (which land on +-448 * 2^e)."""
+    x = small_matrix("wide", 96, 256, 37)
+    q1, s1 = oracle.cast_dim1(x)
+    d = np_bf16_values(oracle.dequant_blocked(q1, oracle.to_blocked(s1)))
+    xt = np_bf16_values(np.ascontiguousarray(x.T))
+    e = np.repeat(s1.astype(np.float64) - 127.0, 32, axis=1)
+    a = np.abs(xt) * np.exp2(-e)
+    with np.errstate(divide="ignore"):
+        step = np.where(a < 2.0 ** -6, 2.0 ** -9, np.exp2(np.floor(np.log2(np.maximum(a, 1e-300))) - 3))
+    unsat = a <= 448.0
+    small = np.abs(d) < 2.0 ** -126       # bf16 subnormal results may round again
+    ok = unsat & ~small
+    assert np.all(np.abs(d - xt)[ok] <= 0.5 * step[ok] * np.exp2(e[ok]))
+    assert np.all(np.abs(d[~unsat]) == 448.0 * np.exp2(e[~unsat]))
