@@ -253,7 +253,7 @@ def make_row(row, args, dev, rank):
     from mxfp8_block_scaled_dim0_gb300 import workloads as W
     u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
 
-    if row in ("fused", "dim1"):
+    if row in ("fused", "dim1", "dim0", "dequant"):
         wl = args.workload or WORKLOAD
         if args.shape:
             M, K = args.shape
@@ -271,6 +271,20 @@ def make_row(row, args, dev, rank):
                         u8(mx.mx_blocked_bytes(K, M // 32)))
             return Row("fused", wl, "mx_cast_kernel<fused2d>", algorithmic_bytes(M, K), 1, build,
                        lambda a, st: mx.mx_cast_dim0_dim1(*a, stream=st), (0,), (1, 2, 3, 4))
+
+        if row == "dim0":
+            def build(i):
+                return (gen(i), torch.empty((M, K), dtype=torch.uint8, device=dev),
+                        u8(mx.mx_blocked_bytes(M, K // 32)))
+            return Row("dim0", wl, "mx_cast_kernel<dim0>", 2 * M * K + M * K + blk(M, K // 32), 1,
+                       build, lambda a, st: mx.mx_cast_dim0(*a, stream=st), (0,), (1, 2))
+        if row == "dequant":
+            # The dim0 copy of the workload (cast once, untimed) back to bf16.
+            def build(i):
+                q, s_blk = mx.cast_dim0(gen(i))
+                return (q, s_blk, torch.empty((M, K), dtype=torch.bfloat16, device=dev))
+            return Row("dequant", wl, "dequant_blocked_kernel", M * K + blk(M, K // 32) + 2 * M * K,
+                       1, build, lambda a, st: mx.mx_dequant_blocked(*a, stream=st), (0, 1), (2,))
 
         def build(i):
             return (gen(i), torch.empty((K, M), dtype=torch.uint8, device=dev),
@@ -294,17 +308,36 @@ def make_row(row, args, dev, rank):
                     torch.empty(G + 1, dtype=torch.int64, device=dev),
                     torch.empty(1, dtype=torch.int32, device=dev))
         nbytes = 2 * M * K + 4 * G + M * K + n0 + M * K + n1 + 16 * (G + 1) + 4
-        return Row("grouped", wl, "group_offsets_kernel + mx_cast_kernel<grouped>", nbytes, 2,
+        # Up to 1024 groups the cast kernel builds its group table itself (one
+        # launch); more groups take the offsets kernel first.
+        one = G <= 1024
+        return Row("grouped", wl, "mx_cast_kernel<grouped>" if one else
+                   "group_offsets_kernel + mx_cast_kernel<grouped>", nbytes, 1 if one else 2,
                    build, lambda a, st: mx.mx_cast_grouped_m(*a, stream=st), (0, 1),
                    (2, 3, 4, 5, 6, 7, 8))
 
-    if row == "experts":
+    if row in ("experts", "experts0", "experts01"):
         wl = args.workload or "experts16x8192x5120"
         E, N, K = W.WORKLOADS[wl].shape
         if args.shape:
             E, N, K = args.shape
             wl = "custom_experts_%dx%dx%d" % (E, N, K)
         ns = mx.mx_3d_scale_bytes(E, N, K)
+        n0 = mx.mx_3d_dim0_scale_bytes(E, N, K)
+        if row == "experts0":
+            def build(i):
+                w = W.experts(E, N, K, 1005 + 100 * i, device=dev)
+                return (w, torch.empty((E, N, K), dtype=torch.uint8, device=dev), u8(n0))
+            return Row("experts0", wl, "mx_cast_kernel<experts0>", 3 * E * N * K + n0, 1, build,
+                       lambda a, st: mx.mx_cast_3d_dim0(*a, stream=st), (0,), (1, 2))
+        if row == "experts01":
+            def build(i):
+                w = W.experts(E, N, K, 1005 + 100 * i, device=dev)
+                return (w, torch.empty((E, N, K), dtype=torch.uint8, device=dev), u8(n0),
+                        torch.empty((K, E * N), dtype=torch.uint8, device=dev), u8(ns))
+            return Row("experts01", wl, "mx_cast_kernel<experts01>", 4 * E * N * K + n0 + ns, 1,
+                       build, lambda a, st: mx.mx_cast_3d_dim0_dim1(*a, stream=st), (0,),
+                       (1, 2, 3, 4))
 
         def build(i):
             w = W.experts(E, N, K, 1005 + 100 * i, device=dev)
@@ -503,7 +536,8 @@ def main(argv=None):
     p.add_argument("--shape", type=int, nargs="+", default=None,
                    help="fused / dim1: M K of a matrix of the same value mix instead; "
                         "experts: E N K; blocked: R C of the scale matrix (profiling)")
-    p.add_argument("--row", choices=["fused", "dim1", "grouped", "experts", "blocked"],
+    p.add_argument("--row", choices=["fused", "dim1", "dim0", "grouped", "experts", "experts0",
+                                     "experts01", "blocked", "dequant"],
                    default="fused", help="which row of the hot path one step runs")
     p.add_argument("--workload", default=None, help="named workload for the row")
     p.add_argument("--graph", action="store_true",

@@ -77,6 +77,17 @@ int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_bl
  * own kernel).  Arguments as in mx_cast_dim0_dim1. */
 int mx_cast_dim1(const void* x, int64_t M, int64_t K, void* q1, void* s1_blk, void* stream);
 
+/* dim0 cast only (the row-major copy and its blocked scales): the dim0 half of
+ * the fused kernel of pytorch/ao PR #1869 (summary), for callers that need
+ * only the K-block copy (a forward-pass operand).
+ *   x       bf16 (M x K), row-major                      [in]
+ *   M, K    M >= 1 (any; dim0 blocks run along K), K % 32 == 0, K >= 32,
+ *           M, K <= 2^31 - 256
+ *   q0      M x K bytes, e4m3                            [out]
+ *   s0_blk  mx_blocked_bytes(M, K/32) bytes, e8m0        [out]
+ * Padding bytes of the blocked buffer are written as zero. */
+int mx_cast_dim0(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, void* stream);
+
 /* Standalone conversion of a plain scale matrix to the blocked layout, the
  * operation of the scale-blocking kernels in pytorch/ao PR #3416 (Changes
  * list) and PR #2990 (perf analysis, scale swizzle kernels).
@@ -128,11 +139,48 @@ int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, 
 int mx_cast_3d_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q1, void* s1_blk,
                     void* stream);
 
+/* dim0 cast of 3D expert weights: blocks of 32 along K, the direction the
+ * forward pass reads the weights in.  The pages cast 3D weights only along N
+ * with the dim1 kernel through the reshape to (E*N, K) (pytorch/ao PR #2990,
+ * perf analysis); this applies the same reshape to the dim0 cast of PR #1869
+ * and blocks each expert's scales on their own, like the dim1 variant.
+ *   w       bf16 (E, N, K)                                       [in]
+ *   E >= 1, N >= 1 (any), K % 32 == 0, K >= 32, E*N and K <= 2^31 - 256
+ *   q0      E x N x K bytes: the dim0 cast of the (E*N, K) matrix [out]
+ *   s0_blk  mx_3d_dim0_scale_bytes(E, N, K) bytes: expert e's (N x K/32)
+ *           scales in blocked layout at byte e * mx_blocked_bytes(N, K/32);
+ *           padding zero                                          [out] */
+int mx_cast_3d_dim0(const void* w, int64_t E, int64_t N, int64_t K, void* q0, void* s0_blk,
+                    void* stream);
+
+/* Both directions of 3D expert weights in one read: mx_cast_3d_dim0's q0 and
+ * s0_blk and mx_cast_3d_dim1's q1 and s1_blk (N % 32 == 0 required, as for
+ * mx_cast_3d_dim1).  Buffer sizes as in those two calls. */
+int mx_cast_3d_dim0_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q0, void* s0_blk,
+                         void* q1, void* s1_blk, void* stream);
+
+/* MX dequantisation to bf16.  The pages define no dequantisation kernel; the
+ * value of an MX element is its scale times its element value (OCP
+ * Microscaling Formats v1.0, MX block definition), here rounded once to bf16
+ * (nearest even; subnormals kept; magnitudes rounding to 2^128 or more give
+ * infinity; a NaN scale (0xFF) or NaN element gives NaN).  Applied to
+ * (q0, s0_blk) of a cast it gives X back up to the cast's rounding; applied
+ * to (q1, s1_blk), with R = K and C = M, it gives X^T.
+ *   q       R x C bytes, e4m3, blocks of 32 along rows      [in]
+ *   R, C    R >= 1, C % 32 == 0, C >= 32, R, C <= 2^31 - 256
+ *   s_blk   mx_blocked_bytes(R, C/32) bytes, e8m0           [in]
+ *   out     R x C bf16                                      [out] */
+int mx_dequant_blocked(const void* q, int64_t R, int64_t C, const void* s_blk, void* out,
+                       void* stream);
+
 /* Size helpers (host only, no CUDA calls).  Return -1 for invalid sizes. */
 int64_t mx_blocked_bytes(int64_t R, int64_t C);
 /* dim 0: (M + 128*G) * ceil4(K/32); dim 1: ceil128(K) * (ceil(M/32) + 4*G). */
 int64_t mx_grouped_m_scale_bytes(int64_t M, int64_t K, int32_t G, int32_t dim);
+/* E * mx_blocked_bytes(K, N/32): dim1 scales of 3D weights. */
 int64_t mx_3d_scale_bytes(int64_t E, int64_t N, int64_t K);
+/* E * mx_blocked_bytes(N, K/32): dim0 scales of 3D weights. */
+int64_t mx_3d_dim0_scale_bytes(int64_t E, int64_t N, int64_t K);
 
 /* Text for an MX_* code (static storage). */
 const char* mx_strerror(int code);

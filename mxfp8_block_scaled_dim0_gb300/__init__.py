@@ -7,9 +7,10 @@ CUDA stream; every step of the cast runs in the library's CUDA kernels.  There
 is no CPU fallback: if the library has not been built, importing the binding
 raises.
 
-Convenience wrappers (``cast_dim0_dim1``, ``cast_dim1``, ``cast_grouped_m``,
-``cast_3d_dim1``, ``scales_to_blocked``) allocate outputs with torch and call
-the same entry points.
+Convenience wrappers (``cast_dim0_dim1``, ``cast_dim0``, ``cast_dim1``,
+``cast_grouped_m``, ``cast_3d_dim1``, ``cast_3d_dim0``, ``cast_3d_dim0_dim1``,
+``scales_to_blocked``, ``dequant_blocked``) allocate outputs with torch and
+call the same entry points.
 """
 import ctypes
 import os
@@ -28,9 +29,11 @@ MX_ERR_GROUPS = -5
 
 # Every function the header declares, for load checks.
 ABI_SYMBOLS = (
-    "mx_cast_dim0_dim1", "mx_cast_dim1", "mx_scales_to_blocked", "mx_cast_grouped_m",
-    "mx_cast_3d_dim1", "mx_blocked_bytes", "mx_grouped_m_scale_bytes", "mx_3d_scale_bytes",
-    "mx_strerror", "mx_last_cuda_error", "mx_watchdog", "mx_selftest_watchdog",
+    "mx_cast_dim0_dim1", "mx_cast_dim0", "mx_cast_dim1", "mx_scales_to_blocked",
+    "mx_cast_grouped_m", "mx_cast_3d_dim1", "mx_cast_3d_dim0", "mx_cast_3d_dim0_dim1",
+    "mx_dequant_blocked", "mx_blocked_bytes", "mx_grouped_m_scale_bytes", "mx_3d_scale_bytes",
+    "mx_3d_dim0_scale_bytes", "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
+    "mx_selftest_watchdog",
 )
 
 
@@ -58,13 +61,18 @@ def _lib():
         P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
         sig = {
             "mx_cast_dim0_dim1": ([P, I64, I64, P, P, P, P, P], ctypes.c_int),
+            "mx_cast_dim0": ([P, I64, I64, P, P, P], ctypes.c_int),
             "mx_cast_dim1": ([P, I64, I64, P, P, P], ctypes.c_int),
             "mx_scales_to_blocked": ([P, I64, I64, P, P], ctypes.c_int),
             "mx_cast_grouped_m": ([P, I64, I64, P, I32, P, P, P, P, P, P, P, P], ctypes.c_int),
             "mx_cast_3d_dim1": ([P, I64, I64, I64, P, P, P], ctypes.c_int),
+            "mx_cast_3d_dim0": ([P, I64, I64, I64, P, P, P], ctypes.c_int),
+            "mx_cast_3d_dim0_dim1": ([P, I64, I64, I64, P, P, P, P, P], ctypes.c_int),
+            "mx_dequant_blocked": ([P, I64, I64, P, P, P], ctypes.c_int),
             "mx_blocked_bytes": ([I64, I64], I64),
             "mx_grouped_m_scale_bytes": ([I64, I64, I32, I32], I64),
             "mx_3d_scale_bytes": ([I64, I64, I64], I64),
+            "mx_3d_dim0_scale_bytes": ([I64, I64, I64], I64),
             "mx_strerror": ([ctypes.c_int], ctypes.c_char_p),
             "mx_last_cuda_error": ([], ctypes.c_int),
             "mx_watchdog": ([ctypes.c_int], ctypes.c_int),
@@ -130,6 +138,10 @@ def mx_3d_scale_bytes(E, N, K):
     return int(_lib().mx_3d_scale_bytes(E, N, K))
 
 
+def mx_3d_dim0_scale_bytes(E, N, K):
+    return int(_lib().mx_3d_dim0_scale_bytes(E, N, K))
+
+
 # ---- entry points (same names as the C ABI) ----------------------------------
 
 def mx_cast_dim0_dim1(x, q0, s0_blk, q1, s1_blk, stream=None):
@@ -142,6 +154,15 @@ def mx_cast_dim0_dim1(x, q0, s0_blk, q1, s1_blk, stream=None):
     _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), 1)
     _check(_lib().mx_cast_dim0_dim1(_ptr(x), M, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
                                     _ptr(s1_blk), _stream(stream)), "mx_cast_dim0_dim1")
+
+
+def mx_cast_dim0(x, q0, s0_blk, stream=None):
+    _dev_tensor(x, "x", itemsize=2)
+    M, K = x.shape
+    _dev_tensor(q0, "q0", M * K, 1)
+    _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), 1)
+    _check(_lib().mx_cast_dim0(_ptr(x), M, K, _ptr(q0), _ptr(s0_blk), _stream(stream)),
+           "mx_cast_dim0")
 
 
 def mx_cast_dim1(x, q1, s1_blk, stream=None):
@@ -189,6 +210,37 @@ def mx_cast_3d_dim1(w, q1, s1_blk, stream=None):
            "mx_cast_3d_dim1")
 
 
+def mx_cast_3d_dim0(w, q0, s0_blk, stream=None):
+    _dev_tensor(w, "w", itemsize=2)
+    E, N, K = w.shape
+    _dev_tensor(q0, "q0", E * N * K, 1)
+    _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), 1)
+    _check(_lib().mx_cast_3d_dim0(_ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk), _stream(stream)),
+           "mx_cast_3d_dim0")
+
+
+def mx_cast_3d_dim0_dim1(w, q0, s0_blk, q1, s1_blk, stream=None):
+    _dev_tensor(w, "w", itemsize=2)
+    E, N, K = w.shape
+    _dev_tensor(q0, "q0", E * N * K, 1)
+    _dev_tensor(q1, "q1", E * N * K, 1)
+    _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), 1)
+    _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), 1)
+    _check(_lib().mx_cast_3d_dim0_dim1(_ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
+                                       _ptr(s1_blk), _stream(stream)), "mx_cast_3d_dim0_dim1")
+
+
+def mx_dequant_blocked(q, s_blk, out, stream=None):
+    """bf16 out (R x C) = e4m3 q (R x C) times 2^(scale - 127), scales in
+    blocked layout."""
+    _dev_tensor(q, "q", itemsize=1)
+    R, C = q.shape
+    _dev_tensor(s_blk, "s_blk", mx_blocked_bytes(R, C // 32), 1)
+    _dev_tensor(out, "out", 2 * R * C, 2)
+    _check(_lib().mx_dequant_blocked(_ptr(q), R, C, _ptr(s_blk), _ptr(out), _stream(stream)),
+           "mx_dequant_blocked")
+
+
 def mx_selftest_watchdog(wait_ns=50_000_000, stream=None):
     """Run the bounded-wait failure path on the device (no fault): a warp
     waits on a barrier that never completes and gives up after wait_ns."""
@@ -217,6 +269,14 @@ def cast_dim0_dim1(x, stream=None):
     s1 = _u8(mx_blocked_bytes(K, M // 32), x.device)
     mx_cast_dim0_dim1(x, q0, s0, q1, s1, stream)
     return q0, s0, q1, s1
+
+
+def cast_dim0(x, stream=None):
+    M, K = x.shape
+    q0 = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s0 = _u8(mx_blocked_bytes(M, K // 32), x.device)
+    mx_cast_dim0(x, q0, s0, stream)
+    return q0, s0
 
 
 def cast_dim1(x, stream=None):
@@ -257,3 +317,31 @@ def cast_3d_dim1(w, stream=None):
     s1 = _u8(mx_3d_scale_bytes(E, N, K), w.device)
     mx_cast_3d_dim1(w, q1, s1, stream)
     return q1, s1
+
+
+def cast_3d_dim0(w, stream=None):
+    """Returns (q0 (E, N, K), s0_blk) as uint8 tensors."""
+    E, N, K = w.shape
+    q0 = torch.empty((E, N, K), dtype=torch.uint8, device=w.device)
+    s0 = _u8(mx_3d_dim0_scale_bytes(E, N, K), w.device)
+    mx_cast_3d_dim0(w, q0, s0, stream)
+    return q0, s0
+
+
+def cast_3d_dim0_dim1(w, stream=None):
+    """Returns (q0 (E, N, K), s0_blk, q1 (K, E*N), s1_blk)."""
+    E, N, K = w.shape
+    q0 = torch.empty((E, N, K), dtype=torch.uint8, device=w.device)
+    q1 = torch.empty((K, E * N), dtype=torch.uint8, device=w.device)
+    s0 = _u8(mx_3d_dim0_scale_bytes(E, N, K), w.device)
+    s1 = _u8(mx_3d_scale_bytes(E, N, K), w.device)
+    mx_cast_3d_dim0_dim1(w, q0, s0, q1, s1, stream)
+    return q0, s0, q1, s1
+
+
+def dequant_blocked(q, s_blk, stream=None):
+    """bf16 tensor of the same shape as the 2D uint8 tensor q."""
+    R, C = q.shape
+    out = torch.empty((R, C), dtype=torch.bfloat16, device=q.device)
+    mx_dequant_blocked(q, s_blk, out, stream)
+    return out

@@ -140,6 +140,44 @@ int launch_rc(int rc) { return rc ? cuda_fail(rc) : MX_OK; }
 
 }  // namespace
 
+namespace {
+
+// Shared body of the 3D casts: q0 / s0_blk null for dim1 only, q1 / s1_blk
+// null for dim0 only.
+int cast_3d(const void* w, int64_t E, int64_t N, int64_t K, void* q0, void* s0_blk, void* q1,
+            void* s1_blk, void* stream) {
+  const bool dim1 = q1 != nullptr;
+  if (E < 1 || N < 1 || K < 32 || K % 32 != 0) return MX_ERR_SHAPE;
+  if (dim1 && (N < 32 || N % 32 != 0)) return MX_ERR_SHAPE;
+  if (N > kMaxDim || E > kMaxDim / N || K > kMaxDim) return MX_ERR_SHAPE;
+  if (!aligned(w, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16) || !aligned(q1, 16) ||
+      !aligned(s1_blk, 16))
+    return MX_ERR_ALIGN;
+  const int64_t M = E * N;
+  mx::CastMaps maps;
+  if (int rc = encode_cast_maps(&maps, w, M, K, q1)) return rc;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (N % 128 != 0) {
+    // Scales are scattered byte by byte in this case; the padding of each
+    // expert's blocked matrices is cleared first.
+    if (s0_blk) {
+      cudaError_t e =
+          cudaMemsetAsync(s0_blk, 0, static_cast<size_t>(mx_3d_dim0_scale_bytes(E, N, K)), st);
+      if (e != cudaSuccess) return cuda_fail(static_cast<int>(e));
+    }
+    if (s1_blk) {
+      cudaError_t e =
+          cudaMemsetAsync(s1_blk, 0, static_cast<size_t>(mx_3d_scale_bytes(E, N, K)), st);
+      if (e != cudaSuccess) return cuda_fail(static_cast<int>(e));
+    }
+  }
+  return launch_rc(mx::launch_cast_experts(maps, E, N, K, q0, s0_blk, s1_blk, sms, st));
+}
+
+}  // namespace
+
 extern "C" {
 
 int64_t mx_blocked_bytes(int64_t R, int64_t C) {
@@ -156,6 +194,11 @@ int64_t mx_grouped_m_scale_bytes(int64_t M, int64_t K, int32_t G, int32_t dim) {
 int64_t mx_3d_scale_bytes(int64_t E, int64_t N, int64_t K) {
   if (E < 0 || N < 0 || K < 0) return -1;
   return E * mx_blocked_bytes(K, N / 32);
+}
+
+int64_t mx_3d_dim0_scale_bytes(int64_t E, int64_t N, int64_t K) {
+  if (E < 0 || N < 0 || K < 0) return -1;
+  return E * mx_blocked_bytes(N, K / 32);
 }
 
 const char* mx_strerror(int code) {
@@ -212,6 +255,31 @@ int mx_cast_dim1(const void* x, int64_t M, int64_t K, void* q1, void* s1_blk, vo
                                       static_cast<cudaStream_t>(stream)));
 }
 
+int mx_cast_dim0(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, void* stream) {
+  if (!x || !q0 || !s0_blk) return MX_ERR_NULL;
+  if (M < 1 || K < 32 || M > kMaxDim || K > kMaxDim || K % 32 != 0) return MX_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16)) return MX_ERR_ALIGN;
+  mx::CastMaps maps;
+  if (int rc = encode_cast_maps(&maps, x, M, K, nullptr)) return rc;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  return launch_rc(mx::launch_cast_2d(maps, M, K, q0, s0_blk, nullptr, sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int mx_dequant_blocked(const void* q, int64_t R, int64_t C, const void* s_blk, void* out,
+                       void* stream) {
+  if (!q || !s_blk || !out) return MX_ERR_NULL;
+  if (R < 1 || C < 32 || R > kMaxDim || C > kMaxDim || C % 32 != 0) return MX_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(s_blk, 16) || !aligned(out, 16)) return MX_ERR_ALIGN;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  return launch_rc(mx::launch_dequant_blocked(static_cast<const uint8_t*>(q), R, C,
+                                              static_cast<const uint8_t*>(s_blk),
+                                              static_cast<uint16_t*>(out), sms,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int mx_scales_to_blocked(const void* s, int64_t R, int64_t C, void* out, void* stream) {
   if (!s || !out) return MX_ERR_NULL;
   if (R < 1 || C < 1 || R > int64_t{65535} * 128 || C > kMaxDim) return MX_ERR_SHAPE;
@@ -249,22 +317,19 @@ int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, 
 int mx_cast_3d_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q1, void* s1_blk,
                     void* stream) {
   if (!w || !q1 || !s1_blk) return MX_ERR_NULL;
-  if (E < 1 || N < 32 || N % 32 != 0 || K < 32 || K % 32 != 0) return MX_ERR_SHAPE;
-  if (N > kMaxDim || E > kMaxDim / N || K > kMaxDim) return MX_ERR_SHAPE;
-  if (!aligned(w, 16) || !aligned(q1, 16) || !aligned(s1_blk, 16)) return MX_ERR_ALIGN;
-  const int64_t M = E * N;
-  mx::CastMaps maps;
-  if (int rc = encode_cast_maps(&maps, w, M, K, q1)) return rc;
-  int sms = 0;
-  if (int rc = current_sm_count(&sms)) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (N % 128 != 0) {
-    // Scales are scattered byte by byte in this case; the padding of each
-    // expert's blocked matrix is cleared first.
-    cudaError_t e = cudaMemsetAsync(s1_blk, 0, static_cast<size_t>(mx_3d_scale_bytes(E, N, K)), st);
-    if (e != cudaSuccess) return cuda_fail(static_cast<int>(e));
-  }
-  return launch_rc(mx::launch_cast_experts(maps, E, N, K, s1_blk, sms, st));
+  return cast_3d(w, E, N, K, nullptr, nullptr, q1, s1_blk, stream);
+}
+
+int mx_cast_3d_dim0(const void* w, int64_t E, int64_t N, int64_t K, void* q0, void* s0_blk,
+                    void* stream) {
+  if (!w || !q0 || !s0_blk) return MX_ERR_NULL;
+  return cast_3d(w, E, N, K, q0, s0_blk, nullptr, nullptr, stream);
+}
+
+int mx_cast_3d_dim0_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q0, void* s0_blk,
+                         void* q1, void* s1_blk, void* stream) {
+  if (!w || !q0 || !s0_blk || !q1 || !s1_blk) return MX_ERR_NULL;
+  return cast_3d(w, E, N, K, q0, s0_blk, q1, s1_blk, stream);
 }
 
 }  // extern "C"

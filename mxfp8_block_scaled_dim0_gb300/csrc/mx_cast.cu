@@ -78,7 +78,27 @@ constexpr int kSmemBytes = kSmemUsed + 1024;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-enum Mode : int { kModeFused2D = 0, kModeDim1 = 1, kModeExperts = 2, kModeGrouped = 3 };
+// Modes: which copies a launch writes and where its scale tiles go.
+//   kModeFused2D   dim0 + dim1, 2D blocked scales
+//   kModeDim1      dim1 only
+//   kModeDim0      dim0 only
+//   kModeExperts   3D weights (E, N, K) as the (E*N, K) matrix: dim1, each
+//                  expert's scales blocked on their own
+//   kModeExperts0  the same for dim0
+//   kModeExperts01 the same for dim0 + dim1
+//   kModeGrouped   grouped-M activations: dim0 + dim1 per group
+enum Mode : int {
+  kModeFused2D = 0, kModeDim1 = 1, kModeExperts = 2, kModeGrouped = 3,
+  kModeDim0 = 4, kModeExperts0 = 5, kModeExperts01 = 6
+};
+__host__ __device__ constexpr bool has_dim0(int m) {
+  return m == kModeFused2D || m == kModeGrouped || m == kModeDim0 || m == kModeExperts0 ||
+         m == kModeExperts01;
+}
+__host__ __device__ constexpr bool has_dim1(int m) { return m != kModeDim0 && m != kModeExperts0; }
+__host__ __device__ constexpr bool per_expert(int m) {
+  return m == kModeExperts || m == kModeExperts0 || m == kModeExperts01;
+}
 
 // One store warp drains a staging buffer by TMA in the 2D / 3D modes.  In
 // the grouped mode q1 cannot leave by TMA (group starts are not 16-byte
@@ -112,6 +132,9 @@ struct Params {
   int64_t s1_expert_bytes;  // blk(K, N/32)
   int32_t s1_scatter;       // N % 128 != 0: scales written byte by byte
   int32_t nb4;              // ceil4(N / 32)
+  int64_t s0_expert_bytes;  // blk(N, K/32)
+  int32_t s0_scatter;       // N % 128 != 0: dim0 scales written byte by byte
+  int32_t kb4;              // ceil4(K / 32)
   // grouped
   const int32_t* offs;
   const int64_t* row_offs;  // s0_row_offs (G + 1), from group_offsets_kernel (G > kMaxSmemGroups)
@@ -179,8 +202,13 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, i
     T.m0 = tm * kTile;
     T.k0 = tk * kTile;
     T.rows = kTile;
-    T.s0_dst = p.s0 ? p.s0 + t * kScaleTile : nullptr;
-    if (kMode == kModeExperts) {
+    // Per-expert dim0 scales with N % 128 == 0 sit exactly where the 2D
+    // layout puts them (expert e's blk(N, K/32) bytes start at tile row e*N/128).
+    T.s0_dst = has_dim0(kMode) && !(per_expert(kMode) && p.s0_scatter) ? p.s0 + t * kScaleTile
+                                                                       : nullptr;
+    if (!has_dim1(kMode)) {
+      T.s1_dst = nullptr;
+    } else if (per_expert(kMode)) {
       if (p.s1_scatter) {
         T.s1_dst = nullptr;
       } else {
@@ -207,9 +235,13 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, i
 //     their maxima with one shuffle.
 // Rows at or beyond `rows` (grouped mode: past the group's end) are neither
 // stored nor given a scale (their blocked scale byte is padding, 0).
+// kScatter (3D weights with N % 128 != 0): a tile can straddle two experts, so
+// each scale byte goes straight to its expert's blocked matrix in global
+// memory instead of the tile's staging.
+template <bool kScatter>
 __device__ __forceinline__ void dim0_half_unit(const uint8_t* in, uint8_t* sc0, uint8_t* q0,
                                                int64_t M, int64_t K, int m0, int k0, int R0,
-                                               int lane, int rows) {
+                                               int lane, int rows, const Params& p) {
   const int row = R0 + ((lane >> 2) & 1) + 2 * (lane >> 4);
   const int box = (lane >> 3) & 1;
   const int hq = lane & 3;
@@ -232,8 +264,17 @@ __device__ __forceinline__ void dim0_half_unit(const uint8_t* in, uint8_t* sc0, 
   const int64_t gr = static_cast<int64_t>(m0) + row;
   const int64_t gc = static_cast<int64_t>(k0) + 64 * box + 16 * hq;
   if (row < rows && gr < M && gc < K) *reinterpret_cast<uint4*>(q0 + gr * K + gc) = o;
-  if ((hq & 1) == 0)
-    sc0[blocked_in_tile(row, 2 * box + (hq >> 1))] = static_cast<uint8_t>(row < rows ? sbyte : 0u);
+  if ((hq & 1) == 0) {
+    if (kScatter) {
+      if (gr < M && gc < K) {
+        const uint32_t e = static_cast<uint32_t>(gr) / static_cast<uint32_t>(p.N);
+        const int64_t n = gr - static_cast<int64_t>(e) * p.N;
+        p.s0[e * p.s0_expert_bytes + blocked_offset(n, gc >> 5, p.kb4)] = static_cast<uint8_t>(sbyte);
+      }
+    } else {
+      sc0[blocked_in_tile(row, 2 * box + (hq >> 1))] = static_cast<uint8_t>(row < rows ? sbyte : 0u);
+    }
+  }
 }
 
 // Four consecutive rows of one column of a dim1 unit -> four e4m3 bytes.
@@ -453,8 +494,9 @@ template <int kMode>
 __global__ void __launch_bounds__(threads_of(kMode), 1)
     mx_cast_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q1e,
                    const __grid_constant__ CUtensorMap tm_q1o, const Params p) {
-  constexpr bool kDim0 = (kMode == kModeFused2D || kMode == kModeGrouped);
-  constexpr bool kTmaQ1 = (kMode != kModeGrouped);
+  constexpr bool kDim0 = has_dim0(kMode);
+  constexpr bool kDim1 = has_dim1(kMode);
+  constexpr bool kTmaQ1 = kDim1 && kMode != kModeGrouped;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -620,12 +662,13 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
           copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows, cont_prev,
                       cont_next, sw, lane);
         }
-      } else if (lane == 0) {
+      } else if (kDim1 && lane == 0) {
         tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, q1s);
         tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, q1s + kQ1Half);
       }
       if (sw == 0) {
-        if (lane == 0 && kDim0) bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
+        if (lane == 0 && kDim0 && T.s0_dst)
+          bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
         if (T.s1_dst) {
           // dim1 scales are staged as [M-block][column]; storage row `lane` of
           // the blocked tile holds columns lane, lane+32, lane+64, lane+96,
@@ -672,19 +715,29 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       uint8_t* sc1 = smem + kOffS1 + o * kScaleTile;
       if (kDim0) {
         uint8_t* sc0 = smem + kOffS0 + o * kScaleTile;
+        if (per_expert(kMode) && p.s0_scatter) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          dim0_half_unit(in, sc0, p.q0, p.M, p.K, T.m0, T.k0, (4 * warp + u) * 4, lane, T.rows);
+          for (int u = 0; u < 4; ++u)
+            dim0_half_unit<true>(in, sc0, p.q0, p.M, p.K, T.m0, T.k0, (4 * warp + u) * 4, lane,
+                                 T.rows, p);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dim0_half_unit<false>(in, sc0, p.q0, p.M, p.K, T.m0, T.k0, (4 * warp + u) * 4, lane,
+                                  T.rows, p);
+        }
       }
       const int mb = warp >> 1;
       const int pcol = (warp & 1) * 32 + lane;
-      uint32_t sb;
-      if (kMode == kModeGrouped && T.rows < kTile)
+      uint32_t sb = 0;
+      if (!kDim1)
+        ;
+      else if (kMode == kModeGrouped && T.rows < kTile)
         sb = dim1_unit<true>(in, q1s, sc1, pcol, mb, T.rows);
       else
         sb = dim1_unit<false>(in, q1s, sc1, pcol, mb, T.rows);
 
-      if (kMode == kModeExperts && T.s1_dst == nullptr) {
+      if (kDim1 && per_expert(kMode) && T.s1_dst == nullptr) {
         // 3D weights with N % 128 != 0: a tile can straddle two experts, so
         // each scale byte goes straight to its expert's blocked matrix.
         const int64_t mbg = (static_cast<int64_t>(T.m0) >> 5) + mb;
@@ -770,6 +823,7 @@ int threads_cast() { return threads_of(kModeFused2D); }
 int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0, void* s1,
                    int num_sms, cudaStream_t stream) {
   const bool dim0 = q0 != nullptr;
+  const bool dim1 = s1 != nullptr;
   Params prm = {};
   prm.q0 = static_cast<uint8_t*>(q0);
   prm.M = M;
@@ -781,13 +835,21 @@ int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s
   prm.s1 = static_cast<uint8_t*>(s1);
   const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
   if (grid <= 0) return 0;
-  return dim0 ? launch<kModeFused2D>(maps, prm, grid, stream)
+  if (dim0 && dim1) return launch<kModeFused2D>(maps, prm, grid, stream);
+  return dim0 ? launch<kModeDim0>(maps, prm, grid, stream)
               : launch<kModeDim1>(maps, prm, grid, stream);
 }
 
-int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* s1,
-                        int num_sms, cudaStream_t stream) {
+int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* q0,
+                        void* s0, void* s1, int num_sms, cudaStream_t stream) {
+  const bool dim0 = q0 != nullptr;
+  const bool dim1 = s1 != nullptr;
   Params prm = {};
+  prm.q0 = static_cast<uint8_t*>(q0);
+  prm.s0 = static_cast<uint8_t*>(s0);
+  prm.kb4 = static_cast<int32_t>(((K / 32) + 3) / 4 * 4);
+  prm.s0_expert_bytes = (N + 127) / 128 * 128 * prm.kb4;
+  prm.s0_scatter = (N % 128) != 0;
   prm.M = E * N;
   prm.K = K;
   prm.n_mt = static_cast<int32_t>((prm.M + kTile - 1) / kTile);
@@ -800,7 +862,9 @@ int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, v
   prm.s1_scatter = (N % 128) != 0;
   const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
   if (grid <= 0) return 0;
-  return launch<kModeExperts>(maps, prm, grid, stream);
+  if (dim0 && dim1) return launch<kModeExperts01>(maps, prm, grid, stream);
+  return dim0 ? launch<kModeExperts0>(maps, prm, grid, stream)
+              : launch<kModeExperts>(maps, prm, grid, stream);
 }
 
 int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_t* offs, int G,

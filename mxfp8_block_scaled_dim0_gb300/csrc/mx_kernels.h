@@ -24,11 +24,17 @@ int smem_bytes_cast();
 int threads_cast();
 
 // All launchers return 0 or a cudaError_t value.
-// q0 == nullptr: dim1 only.
+// q0 == nullptr: dim1 only; s1 == nullptr: dim0 only.
 int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0, void* s1,
                    int num_sms, cudaStream_t stream);
-int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* s1,
-                        int num_sms, cudaStream_t stream);
+// 3D weights (E, N, K) as the (E*N, K) matrix, scales blocked per expert;
+// same null conventions.  With N % 128 != 0 the scales are scattered byte by
+// byte and the caller clears the scale buffers first.
+int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* q0,
+                        void* s0, void* s1, int num_sms, cudaStream_t stream);
+// MX dequantisation (mx_dequant.cu).
+int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t* s_blk,
+                           uint16_t* out, int num_sms, cudaStream_t stream);
 // G <= kMaxSmemGroups: one kernel builds the group table itself; larger G:
 // group_offsets_kernel first, then the cast kernel as its programmatic
 // dependent.

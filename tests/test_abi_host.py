@@ -114,3 +114,23 @@ def test_product_path_does_not_import_oracle():
 def test_selftest_watchdog_rejects_bad_limits(lib):
     assert lib.mx_selftest_watchdog(0, None) == mx.MX_ERR_SHAPE
     assert lib.mx_selftest_watchdog(10**11, None) == mx.MX_ERR_SHAPE
+
+
+def test_new_entry_points_reject_bad_arguments(lib):
+    assert mx.mx_3d_dim0_scale_bytes(16, 8192, 5120) == 16 * 8192 * 160
+    assert mx.mx_3d_dim0_scale_bytes(2, 50, 96) == 2 * 128 * 4
+    assert lib.mx_cast_dim0(None, 64, 64, A, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_dim0(A, 0, 64, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_dim0(A, 64, 48, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_dim0(A, 64, 64, B, A, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_3d_dim0(A, 2, 64, 64, None, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_3d_dim0(A, 2, 0, 64, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_3d_dim0(A, 2, 64, 40, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_3d_dim0(A, 2, 64, 64, A, B, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_3d_dim0_dim1(A, 2, 64, 64, A, A, None, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_3d_dim0_dim1(A, 2, 50, 64, A, A, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_3d_dim0_dim1(A, 2, 64, 64, A, A, B, A, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_dequant_blocked(A, 64, 64, None, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_dequant_blocked(A, 0, 64, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_dequant_blocked(A, 64, 48, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_dequant_blocked(A, 64, 64, A, B, None) == mx.MX_ERR_ALIGN
