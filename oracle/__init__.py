@@ -65,6 +65,10 @@ def _load():
         lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_dequant_blocked.argtypes = [P, I64, I64, P, P]
         lib.oracle_dequant_blocked.restype = ctypes.c_int
+        lib.oracle_cast_tensorwise.argtypes = [P, I64, P, P, P]
+        lib.oracle_cast_tensorwise.restype = None
+        lib.oracle_cast_rowwise.argtypes = [P, I64, I64, P, P]
+        lib.oracle_cast_rowwise.restype = None
         _lib = lib
     return _lib
 
@@ -256,6 +260,30 @@ def dequant_blocked(q, s_blk):
     return out
 
 
+# ---- tensorwise and rowwise fp8 ---------------------------------------------
+
+def cast_tensorwise(x):
+    """bf16 bits (any shape) -> (q uint8 of the same shape, scale float32,
+    amax float32): one scale 448 / amax for the whole tensor."""
+    x = _bits(x)
+    q = np.empty(x.shape, np.uint8)
+    scale = np.zeros(1, np.float32)
+    amax = np.zeros(1, np.float32)
+    _load().oracle_cast_tensorwise(_ptr(x), x.size, _ptr(q), _ptr(scale), _ptr(amax))
+    return q, scale[0], amax[0]
+
+
+def cast_rowwise(x):
+    """(M, K) bf16 bits -> (q (M, K) uint8, scale (M,) bf16 bits): one scale
+    amax / 448 per row, rounded to bf16."""
+    x = _bits(x)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    scale = np.empty(M, np.uint16)
+    _load().oracle_cast_rowwise(_ptr(x), M, K, _ptr(q), _ptr(scale))
+    return q, scale
+
+
 def library_path() -> str:
     return _build.build()
 
@@ -265,5 +293,5 @@ __all__ = [
     "cast_dim0", "cast_dim1", "blocked_bytes", "to_blocked", "from_blocked",
     "cast_dim0_dim1_blocked", "grouped_m_scale_bytes", "cast_grouped_m",
     "cast_3d_dim1", "cast_3d_dim0", "cast_3d_dim0_dim1", "double_to_bf16",
-    "dequant_blocked", "library_path",
+    "dequant_blocked", "cast_tensorwise", "cast_rowwise", "library_path",
 ]

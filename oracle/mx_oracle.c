@@ -40,6 +40,7 @@
  * nearbyint() in the default round-to-nearest-even mode.
  */
 #include <fenv.h>
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -474,4 +475,85 @@ int oracle_dequant_blocked(const uint8_t *q, int64_t R, int64_t C, const uint8_t
     }
     free(s);
     return 0;
+}
+
+/* ---- tensorwise and rowwise fp8 (non-MX contrast cases) ----------------- */
+
+/* Nearest fp32 to v (the C conversion double -> float rounds to nearest even). */
+static double to_f32(double v)
+{
+    return (double)(float)v;
+}
+
+/* Tensorwise fp8 with one dynamic scale for the whole tensor, as in pytorch/ao
+ * PR #1445 "[float8nocompile] Triton kernels for conversion to float8 dtypes"
+ * (global amax over all elements, then one scale, then the conversion):
+ *   amax  = max |x_i|                                   (exact)
+ *   scale = fp32 nearest to 448 / amax; amax = 0 gives 1; a quotient beyond
+ *           the largest finite fp32 gives the largest finite fp32
+ *   q_i   = e4m3(fp32(x_i * scale)), nearest even, saturated to +-448
+ * x holds n bf16 bit patterns; q gets n bytes.  NaN / Inf inputs follow IEEE
+ * arithmetic through the same formula. */
+void oracle_cast_tensorwise(const uint16_t *x, int64_t n, uint8_t *q, float *scale,
+                            float *amax_out)
+{
+    double amax = 0.0;
+    int nan = 0;
+    for (int64_t i = 0; i < n; i++) {
+        double v = oracle_bf16_to_double(x[i]);
+        if (isnan(v))
+            nan = 1;
+        else if (fabs(v) > amax)
+            amax = fabs(v);
+    }
+    if (nan)
+        amax = NAN;
+    double s;
+    if (amax == 0.0)
+        s = 1.0;
+    else {
+        s = to_f32(E4M3_MAXNORM / amax);
+        if (isinf(s))
+            s = (double)FLT_MAX;
+    }
+    for (int64_t i = 0; i < n; i++)
+        q[i] = oracle_e4m3_rne_sat(to_f32(oracle_bf16_to_double(x[i]) * s));
+    *scale = (float)s;
+    *amax_out = (float)amax;
+}
+
+/* Rowwise fp8 with one scale per row, as in the "FP8 linear triton with
+ * row-wise scaling" gist (quantize_fp8_rowwise):
+ *   amax_r  = max_j |x_rj|                               (exact)
+ *   scale_r = bf16 nearest to amax_r / 448 (the input's dtype)
+ *   q_rj    = e4m3(fp32(x_rj / scale_r)), nearest even, saturated to +-448
+ * A row whose scale is 0 (all zero, or amax_r / 448 below half the smallest
+ * bf16 subnormal) encodes as signed zeros instead of the formula's 0/0.
+ * x is M x K bf16 bits; q gets M x K bytes, scale M bf16 bit patterns. */
+void oracle_cast_rowwise(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, uint16_t *scale)
+{
+    for (int64_t r = 0; r < M; r++) {
+        const uint16_t *xr = x + r * K;
+        double amax = 0.0;
+        int nan = 0;
+        for (int64_t j = 0; j < K; j++) {
+            double v = oracle_bf16_to_double(xr[j]);
+            if (isnan(v))
+                nan = 1;
+            else if (fabs(v) > amax)
+                amax = fabs(v);
+        }
+        if (nan)
+            amax = NAN;
+        uint16_t sb = oracle_double_to_bf16(amax / E4M3_MAXNORM);
+        double s = oracle_bf16_to_double(sb);
+        scale[r] = sb;
+        for (int64_t j = 0; j < K; j++) {
+            double v = oracle_bf16_to_double(xr[j]);
+            if (s == 0.0)
+                q[r * K + j] = signbit(v) ? 0x80 : 0x00;
+            else
+                q[r * K + j] = oracle_e4m3_rne_sat(to_f32(v / s));
+        }
+    }
 }

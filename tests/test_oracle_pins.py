@@ -464,3 +464,88 @@ def test_dequant_of_cast_is_within_half_ulp():
     ok = unsat & ~small
     assert np.all(np.abs(d - xt)[ok] <= 0.5 * step[ok] * np.exp2(e[ok]))
     assert np.all(np.abs(d[~unsat]) == 448.0 * np.exp2(e[~unsat]))
+
+
+# ---- tensorwise and rowwise fp8 ------------------------------------------------
+
+def _golden_scaled():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "hand_worked_scaled_fp8.txt")
+    cases = []
+    for line in open(path):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            kind, xs, sc, qs = [t.strip() for t in line.split("|")]
+            cases.append((kind, [int(v, 16) for v in xs.split()], int(sc, 16),
+                          [int(v, 16) for v in qs.split()]))
+    return cases
+
+
+def test_scaled_fp8_hand_worked():
+    cases = _golden_scaled()
+    assert sum(c[0] == "tensorwise" for c in cases) >= 4 and sum(c[0] == "rowwise" for c in cases) >= 4
+    for kind, xs, sc, qs in cases:
+        x = np.array([xs], np.uint16)
+        if kind == "tensorwise":
+            q, scale, amax = oracle.cast_tensorwise(x)
+            assert np.float32(scale).view(np.uint32) == sc, (xs, hex(np.float32(scale).view(np.uint32)))
+            assert amax == np.abs(np_bf16_values(x)).max()
+        else:
+            q, scale = oracle.cast_rowwise(x)
+            assert scale[0] == sc, (xs, hex(scale[0]))
+        assert list(q.ravel()) == qs, (kind, xs, [hex(v) for v in q.ravel()])
+
+
+def _e4m3_lib(v32):
+    """fp32 values -> e4m3fn bytes by ml_dtypes (nearest even), after
+    saturating to +-448."""
+    v = np.clip(np.asarray(v32, np.float32), -448.0, 448.0)
+    return v.astype(ml_dtypes.float8_e4m3fn).view(np.uint8)
+
+
+@pytest.mark.parametrize("kind", ["spiky", "wide", "normal"])
+def test_tensorwise_against_float32_arithmetic(kind):
+    """The whole cast redone in numpy float32 (IEEE division and product) with
+    ml_dtypes' e4m3 encoder."""
+    x = small_matrix(kind, 96, 160, 41)
+    q, scale, amax = oracle.cast_tensorwise(x)
+    xv = np_bf16_values(x).astype(np.float32)
+    a = np.float32(np.abs(xv).max())
+    assert amax == a
+    s = np.float32(448.0) / a
+    assert scale == s
+    assert np.array_equal(q, _e4m3_lib(xv * s))
+    assert np.abs(q.view(ml_dtypes.float8_e4m3fn).astype(np.float64)).max() == 448.0
+
+
+@pytest.mark.parametrize("kind", ["spiky", "wide", "normal"])
+def test_rowwise_against_float32_arithmetic(kind):
+    """Per row: bf16(amax / 448) by ml_dtypes from the float32 quotient (one
+    rounding to bf16 would give the same, the float32 step being exact to far
+    more bits than bf16 keeps), then the float32 quotient and ml_dtypes' e4m3
+    encoder."""
+    x = small_matrix(kind, 64, 96, 43)
+    q, scale = oracle.cast_rowwise(x)
+    xv = np_bf16_values(x).astype(np.float32)
+    a = np.abs(xv).max(axis=1)
+    s = (a / np.float32(448.0)).astype(ml_dtypes.bfloat16)
+    assert np.array_equal(scale, s.view(np.uint16))
+    sv = s.astype(np.float32)[:, None]
+    nz = (sv != 0).ravel()
+    with np.errstate(divide="ignore", invalid="ignore"):
+        want = _e4m3_lib(xv / sv)
+    assert np.array_equal(q[nz], want[nz])
+    zero_rows = q[~nz]
+    assert np.all((zero_rows & 0x7F) == 0)
+
+
+def test_tensorwise_degenerate_scales():
+    # amax below 448 / FLT_MAX: the quotient overflows fp32 -> largest finite
+    x = np.array([0x0001, 0x8001, 0x0000], np.uint16)          # +-2^-133
+    q, scale, amax = oracle.cast_tensorwise(x)
+    assert scale == np.finfo(np.float32).max
+    # 2^-133 * FLT_MAX ~ 2^-5 -> e4m3 exactly representable? (1-2^-24)*2^-5 -> 2^-5
+    assert list(q) == [0x10, 0x90, 0x00]
+    # all zero -> scale 1
+    q, scale, amax = oracle.cast_tensorwise(np.zeros(8, np.uint16))
+    assert scale == 1.0 and amax == 0.0 and not q.any()
