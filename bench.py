@@ -253,7 +253,7 @@ def make_row(row, args, dev, rank):
     from mxfp8_block_scaled_dim0_gb300 import workloads as W
     u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
 
-    if row in ("fused", "dim1", "dim0", "dequant"):
+    if row in ("fused", "dim1", "dim0", "dequant", "tensorwise", "rowwise"):
         wl = args.workload or WORKLOAD
         if args.shape:
             M, K = args.shape
@@ -278,6 +278,21 @@ def make_row(row, args, dev, rank):
                         u8(mx.mx_blocked_bytes(M, K // 32)))
             return Row("dim0", wl, "mx_cast_kernel<dim0>", 2 * M * K + M * K + blk(M, K // 32), 1,
                        build, lambda a, st: mx.mx_cast_dim0(*a, stream=st), (0,), (1, 2))
+        if row == "tensorwise":
+            # Two passes over x (global amax, then the cast) and the q write.
+            def build(i):
+                return (gen(i), torch.empty((M, K), dtype=torch.uint8, device=dev),
+                        torch.empty(1, dtype=torch.float32, device=dev),
+                        torch.empty(1, dtype=torch.float32, device=dev))
+            return Row("tensorwise", wl, "tensor_amax_kernel + tensorwise_kernel",
+                       2 * M * K + 2 * M * K + M * K + 8, 2, build,
+                       lambda a, st: mx.mx_cast_tensorwise(*a, stream=st), (0,), (1, 2, 3))
+        if row == "rowwise":
+            def build(i):
+                return (gen(i), torch.empty((M, K), dtype=torch.uint8, device=dev),
+                        torch.empty(M, dtype=torch.bfloat16, device=dev))
+            return Row("rowwise", wl, "rowwise_kernel", 2 * M * K + M * K + 2 * M, 1, build,
+                       lambda a, st: mx.mx_cast_rowwise(*a, stream=st), (0,), (1, 2))
         if row == "dequant":
             # The dim0 copy of the workload (cast once, untimed) back to bf16.
             def build(i):
@@ -537,7 +552,7 @@ def main(argv=None):
                    help="fused / dim1: M K of a matrix of the same value mix instead; "
                         "experts: E N K; blocked: R C of the scale matrix (profiling)")
     p.add_argument("--row", choices=["fused", "dim1", "dim0", "grouped", "experts", "experts0",
-                                     "experts01", "blocked", "dequant"],
+                                     "experts01", "blocked", "dequant", "tensorwise", "rowwise"],
                    default="fused", help="which row of the hot path one step runs")
     p.add_argument("--workload", default=None, help="named workload for the row")
     p.add_argument("--graph", action="store_true",

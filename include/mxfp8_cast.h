@@ -173,6 +173,37 @@ int mx_cast_3d_dim0_dim1(const void* w, int64_t E, int64_t N, int64_t K, void* q
 int mx_dequant_blocked(const void* q, int64_t R, int64_t C, const void* s_blk, void* out,
                        void* stream);
 
+/* Tensorwise fp8: one dynamic scale for the whole tensor, the conversion of
+ * pytorch/ao PR #1445 "[float8nocompile] Triton kernels for conversion to
+ * float8 dtypes" (local amaxes in parallel, a global amax, then the
+ * conversion, each block of which computes the scale itself).  Not an MX
+ * format: the contrast case with a non-power-of-two scale.
+ *   amax  = max |x|, written to *amax (fp32; NaN if x holds a NaN)
+ *   scale = fp32 nearest to 448 / amax, written to *scale; amax = 0 gives
+ *           1, a quotient beyond the largest finite fp32 gives that value
+ *   q     = e4m3(fp32(x * scale)), nearest even, saturated to +-448
+ *   x      n bf16 values, any shape, dense                    [in]
+ *   n      >= 1, <= 2^40
+ *   q      n bytes, e4m3                                      [out]
+ *   scale  one fp32, device memory                            [out]
+ *   amax   one fp32, device memory; also the call's reduction
+ *          target (cleared, then reduced into)                [out]
+ * Enqueues a 4-byte memset and two kernels. */
+int mx_cast_tensorwise(const void* x, int64_t n, void* q, float* scale, float* amax,
+                       void* stream);
+
+/* Rowwise fp8: one scale per row, quantize_fp8_rowwise of the "FP8 linear
+ * triton with row-wise scaling" gist.
+ *   scale_r = bf16 nearest to max_j |x_rj| / 448 (bf16, the input's dtype)
+ *   q_rj    = e4m3(fp32(x_rj / scale_r)), nearest even, saturated to +-448;
+ *             a row whose scale is 0 (all zero, or amax below about 2^-125)
+ *             gives signed zeros rather than the formula's 0/0
+ *   x       bf16 (M x K)                                      [in]
+ *   M, K    M >= 1, K >= 8, K % 8 == 0, M, K <= 2^31 - 256
+ *   q       M x K bytes, e4m3                                 [out]
+ *   scale   M bf16 values                                     [out] */
+int mx_cast_rowwise(const void* x, int64_t M, int64_t K, void* q, void* scale, void* stream);
+
 /* Size helpers (host only, no CUDA calls).  Return -1 for invalid sizes. */
 int64_t mx_blocked_bytes(int64_t R, int64_t C);
 /* dim 0: (M + 128*G) * ceil4(K/32); dim 1: ceil128(K) * (ceil(M/32) + 4*G). */

@@ -9,8 +9,8 @@ raises.
 
 Convenience wrappers (``cast_dim0_dim1``, ``cast_dim0``, ``cast_dim1``,
 ``cast_grouped_m``, ``cast_3d_dim1``, ``cast_3d_dim0``, ``cast_3d_dim0_dim1``,
-``scales_to_blocked``, ``dequant_blocked``) allocate outputs with torch and
-call the same entry points.
+``scales_to_blocked``, ``dequant_blocked``, ``cast_tensorwise``,
+``cast_rowwise``) allocate outputs with torch and call the same entry points.
 """
 import ctypes
 import os
@@ -32,7 +32,7 @@ ABI_SYMBOLS = (
     "mx_cast_dim0_dim1", "mx_cast_dim0", "mx_cast_dim1", "mx_scales_to_blocked",
     "mx_cast_grouped_m", "mx_cast_3d_dim1", "mx_cast_3d_dim0", "mx_cast_3d_dim0_dim1",
     "mx_dequant_blocked", "mx_blocked_bytes", "mx_grouped_m_scale_bytes", "mx_3d_scale_bytes",
-    "mx_3d_dim0_scale_bytes", "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
+    "mx_3d_dim0_scale_bytes", "mx_cast_tensorwise", "mx_cast_rowwise", "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
     "mx_selftest_watchdog",
 )
 
@@ -69,6 +69,8 @@ def _lib():
             "mx_cast_3d_dim0": ([P, I64, I64, I64, P, P, P], ctypes.c_int),
             "mx_cast_3d_dim0_dim1": ([P, I64, I64, I64, P, P, P, P, P], ctypes.c_int),
             "mx_dequant_blocked": ([P, I64, I64, P, P, P], ctypes.c_int),
+            "mx_cast_tensorwise": ([P, I64, P, P, P, P], ctypes.c_int),
+            "mx_cast_rowwise": ([P, I64, I64, P, P, P], ctypes.c_int),
             "mx_blocked_bytes": ([I64, I64], I64),
             "mx_grouped_m_scale_bytes": ([I64, I64, I32, I32], I64),
             "mx_3d_scale_bytes": ([I64, I64, I64], I64),
@@ -241,6 +243,28 @@ def mx_dequant_blocked(q, s_blk, out, stream=None):
            "mx_dequant_blocked")
 
 
+def mx_cast_tensorwise(x, q, scale, amax, stream=None):
+    """Tensorwise fp8 of bf16 x (any shape): q (x.numel() bytes), scale and
+    amax (one float32 each)."""
+    _dev_tensor(x, "x", itemsize=2)
+    n = x.numel()
+    _dev_tensor(q, "q", n, 1)
+    _dev_tensor(scale, "scale", 4, 4)
+    _dev_tensor(amax, "amax", 4, 4)
+    _check(_lib().mx_cast_tensorwise(_ptr(x), n, _ptr(q), _ptr(scale), _ptr(amax),
+                                     _stream(stream)), "mx_cast_tensorwise")
+
+
+def mx_cast_rowwise(x, q, scale, stream=None):
+    """Rowwise fp8 of bf16 x (M x K): q (M x K bytes), scale (M bf16)."""
+    _dev_tensor(x, "x", itemsize=2)
+    M, K = x.shape
+    _dev_tensor(q, "q", M * K, 1)
+    _dev_tensor(scale, "scale", 2 * M, 2)
+    _check(_lib().mx_cast_rowwise(_ptr(x), M, K, _ptr(q), _ptr(scale), _stream(stream)),
+           "mx_cast_rowwise")
+
+
 def mx_selftest_watchdog(wait_ns=50_000_000, stream=None):
     """Run the bounded-wait failure path on the device (no fault): a warp
     waits on a barrier that never completes and gives up after wait_ns."""
@@ -345,3 +369,21 @@ def dequant_blocked(q, s_blk, stream=None):
     out = torch.empty((R, C), dtype=torch.bfloat16, device=q.device)
     mx_dequant_blocked(q, s_blk, out, stream)
     return out
+
+
+def cast_tensorwise(x, stream=None):
+    """Returns (q uint8 shaped like x, scale float32 (1,), amax float32 (1,))."""
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    mx_cast_tensorwise(x, q, scale, amax, stream)
+    return q, scale, amax
+
+
+def cast_rowwise(x, stream=None):
+    """Returns (q (M, K) uint8, scale (M,) bfloat16)."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    scale = torch.empty(M, dtype=torch.bfloat16, device=x.device)
+    mx_cast_rowwise(x, q, scale, stream)
+    return q, scale

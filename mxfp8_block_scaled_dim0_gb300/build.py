@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmxfp8_cast.so")
-SOURCES = ["mx_cast.cu", "mx_blocked.cu", "mx_dequant.cu", "mx_abi.cu"]
+SOURCES = ["mx_cast.cu", "mx_blocked.cu", "mx_dequant.cu", "mx_scaled.cu", "mx_abi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

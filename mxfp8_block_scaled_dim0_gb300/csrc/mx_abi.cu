@@ -280,6 +280,30 @@ int mx_dequant_blocked(const void* q, int64_t R, int64_t C, const void* s_blk, v
                                               static_cast<cudaStream_t>(stream)));
 }
 
+int mx_cast_tensorwise(const void* x, int64_t n, void* q, float* scale, float* amax,
+                       void* stream) {
+  if (!x || !q || !scale || !amax) return MX_ERR_NULL;
+  if (n < 1 || n > (int64_t{1} << 40)) return MX_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4) || !aligned(amax, 4))
+    return MX_ERR_ALIGN;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  return launch_rc(mx::launch_cast_tensorwise(static_cast<const uint16_t*>(x), n,
+                                              static_cast<uint8_t*>(q), scale, amax, sms,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int mx_cast_rowwise(const void* x, int64_t M, int64_t K, void* q, void* scale, void* stream) {
+  if (!x || !q || !scale) return MX_ERR_NULL;
+  if (M < 1 || K < 8 || K % 8 != 0 || M > kMaxDim || K > kMaxDim) return MX_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 2)) return MX_ERR_ALIGN;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  return launch_rc(mx::launch_cast_rowwise(static_cast<const uint16_t*>(x), M, K,
+                                           static_cast<uint8_t*>(q), static_cast<uint16_t*>(scale),
+                                           sms, static_cast<cudaStream_t>(stream)));
+}
+
 int mx_scales_to_blocked(const void* s, int64_t R, int64_t C, void* out, void* stream) {
   if (!s || !out) return MX_ERR_NULL;
   if (R < 1 || C < 1 || R > int64_t{65535} * 128 || C > kMaxDim) return MX_ERR_SHAPE;

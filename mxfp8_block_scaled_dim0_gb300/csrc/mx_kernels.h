@@ -32,6 +32,13 @@ int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s
 // byte and the caller clears the scale buffers first.
 int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* q0,
                         void* s0, void* s1, int num_sms, cudaStream_t stream);
+// Tensorwise / rowwise fp8 (mx_scaled.cu).  Tensorwise clears *amax, reduces
+// into it, then casts (amax kernel, then the cast as its programmatic
+// dependent).
+int launch_cast_tensorwise(const uint16_t* x, int64_t n, uint8_t* q, float* scale, float* amax,
+                           int num_sms, cudaStream_t stream);
+int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint16_t* scale,
+                        int num_sms, cudaStream_t stream);
 // MX dequantisation (mx_dequant.cu).
 int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t* s_blk,
                            uint16_t* out, int num_sms, cudaStream_t stream);

@@ -1,0 +1,335 @@
+// mx_scaled.cu -- the non-MX fp8 casts for sm_103a: one scale per tensor
+// (tensorwise) or per row (rowwise), the contrast cases to the MX block cast.
+//
+// Tensorwise (pytorch/ao PR #1445 "[float8nocompile] Triton kernels for
+// conversion to float8 dtypes": local amaxes in parallel, one global amax,
+// then the conversion; the scale computed locally by every block of the
+// conversion kernel, as that discussion proposes):
+//   amax  = max |x|; scale = fp32(448 / amax) (amax = 0 -> 1, overflow ->
+//   the largest finite fp32); q = e4m3(fp32(x * scale)), nearest even,
+//   saturated.
+//   tensor_amax_kernel  one wave of CTAs, 16-byte loads, integer max of the
+//                       bf16 magnitude bits (NaN patterns order above Inf, so
+//                       a NaN anywhere makes the amax NaN), one atomicMax per
+//                       CTA into the caller's amax word (cleared first)
+//   tensorwise_kernel   programmatic dependent of the amax kernel; walks the
+//                       tensor from the end, so the part of x still in L2 from
+//                       the amax pass is read first
+// Rowwise ("FP8 linear triton with row-wise scaling" gist,
+// quantize_fp8_rowwise): scale_r = bf16(amax_r / 448), q = e4m3(fp32(x /
+// scale_r)); a zero scale gives signed zeros.  A group of T threads (32 to
+// 256, by K) owns a row: it reduces the row's amax, keeping its part of the
+// row in registers (up to 8 chunks of 8 values per thread, K <= 16384; longer
+// rows are read again, from L2), then divides and converts.  The division is
+// a reciprocal product with one residual correction, exact for these
+// operands (row_quot_fast).
+//
+// Exactness against a single rounding: the fp32 product of a bf16 value and
+// an fp32 scale is rounded once by mul.rn and once more by the e4m3
+// conversion, as the pages' fp32 arithmetic does; the fp32 quotients (div.rn,
+// IEEE) likewise.  448 / amax and amax / 448 are rounded to fp32 and then (row
+// scale) to bf16; double rounding of a quotient through a format with at least
+// 2p + 2 bits is harmless, so the bf16 scale equals the nearest bf16 to the
+// exact quotient.
+#include <cuda_runtime.h>
+#include <float.h>
+
+#include "mx_common.cuh"
+#include "mx_kernels.h"
+
+namespace mx {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float div_rn(float a, float b) {
+  float r;
+  asm("div.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Two fp32 values -> two e4m3 bytes (lo = a), nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// Largest bf16 magnitude among the eight values of a 16-byte chunk.
+__device__ __forceinline__ uint32_t mag_max8(uint4 v) {
+  const uint32_t m = 0x7FFF7FFFu;
+  const uint32_t a = __vmaxu2(__vmaxu2(v.x & m, v.y & m), __vmaxu2(v.z & m, v.w & m));
+  return max(a & 0xFFFFu, a >> 16);
+}
+
+__device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
+  v = __reduce_max_sync(0xffffffffu, v);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  uint32_t m = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) m = max(m, red[w]);
+  return m;
+}
+
+__global__ void __launch_bounds__(kThreads) tensor_amax_kernel(const uint16_t* x, int64_t n,
+                                                               uint32_t* amax_bits) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ uint32_t red[kThreads / 32];
+  const int64_t chunks = n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  uint32_t m = 0;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; c < chunks;
+       c += 2 * stride) {
+    const bool two = c + stride < chunks;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(x) + c);
+    uint4 b = make_uint4(0, 0, 0, 0);
+    if (two) b = __ldg(reinterpret_cast<const uint4*>(x) + c + stride);
+    m = max(m, max(mag_max8(a), mag_max8(b)));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    for (int64_t i = chunks << 3; i < n; ++i) m = max(m, static_cast<uint32_t>(x[i] & 0x7FFFu));
+  m = block_max(m, red);
+  if (threadIdx.x == 0 && m != 0) atomicMax(amax_bits, m << 16);
+}
+
+__device__ __forceinline__ float tensor_scale(uint32_t amax_bits) {
+  const float a = __uint_as_float(amax_bits);
+  if (a == 0.0f) return 1.0f;
+  const float s = div_rn(448.0f, a);
+  return s > FLT_MAX ? FLT_MAX : s;   // NaN stays NaN
+}
+
+__global__ void __launch_bounds__(kThreads) tensorwise_kernel(const uint16_t* x, int64_t n,
+                                                              const uint32_t* amax_bits,
+                                                              uint8_t* q, float* scale_out) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const float s = tensor_scale(*amax_bits);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *scale_out = s;
+    for (int64_t i = (n >> 3) << 3; i < n; ++i) {
+      const float v = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+      q[i] = static_cast<uint8_t>(e4m3x2(mul_rn(v, s), 0.0f) & 0xFFu);
+    }
+  }
+  const int64_t chunks = n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  // From the last chunk backwards.
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; k < chunks;
+       k += 2 * stride) {
+    const int64_t c0 = chunks - 1 - k;
+    const int64_t c1 = c0 - stride;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(x) + c0);
+    uint4 b = make_uint4(0, 0, 0, 0);
+    if (c1 >= 0) b = __ldg(reinterpret_cast<const uint4*>(x) + c1);
+    uint2 oa, ob;
+    oa.x = e4m3x4(bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y), s);
+    oa.y = e4m3x4(bf_lo(a.z), bf_hi(a.z), bf_lo(a.w), bf_hi(a.w), s);
+    reinterpret_cast<uint2*>(q)[c0] = oa;
+    if (c1 >= 0) {
+      ob.x = e4m3x4(bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y), s);
+      ob.y = e4m3x4(bf_lo(b.z), bf_hi(b.z), bf_lo(b.w), bf_hi(b.w), s);
+      reinterpret_cast<uint2*>(q)[c1] = ob;
+    }
+  }
+}
+
+// x / s for one bf16 value; a zero scale gives a signed zero.
+__device__ __forceinline__ float row_quot(float v, float s) {
+  return s == 0.0f ? __uint_as_float(__float_as_uint(v) & 0x80000000u) : div_rn(v, s);
+}
+
+// x / s for a normal, finite scale s with r = 1/s rounded to nearest: one
+// product and one residual correction (Markstein's division step).  Both
+// operands carry 8-bit significands, so an inexact quotient lies at least
+// 2^-33 (relative) from every fp32 rounding boundary, far outside the ~2^-46
+// error of the corrected quotient: the result is the correctly rounded fp32
+// quotient, exact ones included.  The sign is taken from v so that -0 stays
+// -0 (the residual of a zero is +0).
+__device__ __forceinline__ float row_quot_fast(float v, float s, float r) {
+  const float q1 = mul_rn(v, r);
+  float rem, q2;
+  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(rem) : "f"(-q1), "f"(s), "f"(v));
+  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(q2) : "f"(rem), "f"(r), "f"(q1));
+  return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) | (__float_as_uint(v) & 0x80000000u));
+}
+
+template <bool kFast>
+__device__ __forceinline__ uint32_t row_e4m3x2(uint32_t w, float s, float r) {
+  const float a = bf_lo(w), b = bf_hi(w);
+  return kFast ? e4m3x2(row_quot_fast(a, s, r), row_quot_fast(b, s, r))
+               : e4m3x2(row_quot(a, s), row_quot(b, s));
+}
+
+template <bool kFast>
+__device__ __forceinline__ void row_pass2(const uint4* xr, uint2* qr, int64_t chunks, int tid,
+                                          int T, float s, float r) {
+  for (int64_t c = tid; c < chunks; c += T) {
+    const uint4 a = __ldg(xr + c);
+    uint2 o;
+    o.x = row_e4m3x2<kFast>(a.x, s, r) | (row_e4m3x2<kFast>(a.y, s, r) << 16);
+    o.y = row_e4m3x2<kFast>(a.z, s, r) | (row_e4m3x2<kFast>(a.w, s, r) << 16);
+    qr[c] = o;
+  }
+}
+
+// Row reduction shared by both rowwise variants: the group's amax -> the
+// bf16 scale bits.
+__device__ __forceinline__ uint16_t row_scale(uint32_t m, uint32_t* red, int g, int t_log2) {
+  m = __reduce_max_sync(0xffffffffu, m);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[warp] = m;
+  __syncthreads();
+  const int w0 = (g << t_log2) >> 5;
+  for (int w = 0; w < (1 << (t_log2 - 5)); ++w) m = max(m, red[w0 + w]);
+  __syncthreads();                            // red is reused by the next row step
+  uint16_t sb;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(sb) : "f"(div_rn(__uint_as_float(m << 16), 448.0f)));
+  return sb;
+}
+
+// kHold > 0: each thread keeps its (at most kHold) chunks of the row in
+// registers between the amax reduction and the conversion, so the row is
+// read once.  kHold == 0: rows too long for that are read twice (the second
+// read hits L2).
+template <int kHold>
+__global__ void __launch_bounds__(kThreads) rowwise_kernel(const uint16_t* x, int64_t M,
+                                                           int64_t K, int t_log2, uint8_t* q,
+                                                           uint16_t* scale) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ uint32_t red[kThreads / 32];
+  const int T = 1 << t_log2;                 // threads per row, 32..256
+  const int groups = kThreads >> t_log2;     // rows per CTA step
+  const int g = threadIdx.x >> t_log2;
+  const int tid = threadIdx.x & (T - 1);
+  const int64_t chunks = K >> 3;
+  for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * groups; r0 < M;
+       r0 += static_cast<int64_t>(gridDim.x) * groups) {
+    const int64_t r = r0 + g;
+    const bool live = r < M;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + r * K);
+    uint2* qr = reinterpret_cast<uint2*>(q + r * K);
+    uint32_t m = 0;
+    if (kHold > 0) {
+      uint4 v[kHold > 0 ? kHold : 1];
+#pragma unroll
+      for (int i = 0; i < kHold; ++i) {
+        const int64_t c = tid + static_cast<int64_t>(i) * T;
+        v[i] = live && c < chunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+        m = max(m, mag_max8(v[i]));
+      }
+      const uint16_t sb = row_scale(m, red, g, t_log2);
+      if (!live) continue;
+      const float s = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+      if (tid == 0) scale[r] = sb;
+      const bool fast = s >= FLT_MIN && s <= FLT_MAX;
+      const float rcp = fast ? div_rn(1.0f, s) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < kHold; ++i) {
+        const int64_t c = tid + static_cast<int64_t>(i) * T;
+        if (c >= chunks) break;
+        uint2 o;
+        if (fast) {
+          o.x = row_e4m3x2<true>(v[i].x, s, rcp) | (row_e4m3x2<true>(v[i].y, s, rcp) << 16);
+          o.y = row_e4m3x2<true>(v[i].z, s, rcp) | (row_e4m3x2<true>(v[i].w, s, rcp) << 16);
+        } else {
+          o.x = row_e4m3x2<false>(v[i].x, s, 0.0f) | (row_e4m3x2<false>(v[i].y, s, 0.0f) << 16);
+          o.y = row_e4m3x2<false>(v[i].z, s, 0.0f) | (row_e4m3x2<false>(v[i].w, s, 0.0f) << 16);
+        }
+        qr[c] = o;
+      }
+    } else {
+      if (live) {
+        for (int64_t c = tid; c < chunks; c += 2 * T) {
+          const uint4 a = __ldg(xr + c);
+          uint4 b = make_uint4(0, 0, 0, 0);
+          if (c + T < chunks) b = __ldg(xr + c + T);
+          m = max(m, max(mag_max8(a), mag_max8(b)));
+        }
+      }
+      const uint16_t sb = row_scale(m, red, g, t_log2);
+      if (!live) continue;
+      const float s = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+      if (tid == 0) scale[r] = sb;
+      // Normal finite scales take the reciprocal path; zero, subnormal, Inf
+      // and NaN scales the IEEE division.
+      if (s >= FLT_MIN && s <= FLT_MAX)
+        row_pass2<true>(xr, qr, chunks, tid, T, s, div_rn(1.0f, s));
+      else
+        row_pass2<false>(xr, qr, chunks, tid, T, s, 0.0f);
+    }
+  }
+}
+
+template <typename... Args>
+int launch_pdl(void (*kernel)(Args...), int grid, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
+
+template <typename K>
+int wave(K kernel, int num_sms) {
+  int per = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kThreads, 0) != cudaSuccess ||
+      per < 1)
+    per = 1;
+  return num_sms * per;
+}
+
+}  // namespace
+
+int launch_cast_tensorwise(const uint16_t* x, int64_t n, uint8_t* q, float* scale, float* amax,
+                           int num_sms, cudaStream_t stream) {
+  static const int per_amax = wave(tensor_amax_kernel, 1);
+  static const int per_cast = wave(tensorwise_kernel, 1);
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  const int64_t chunks = (n >> 3) > 0 ? (n >> 3) : 1;
+  const int64_t want_a = static_cast<int64_t>(num_sms) * per_amax;
+  const int64_t want_c = static_cast<int64_t>(num_sms) * per_cast;
+  const int ga = static_cast<int>(chunks < want_a ? chunks : want_a);
+  const int gc = static_cast<int>(chunks < want_c ? chunks : want_c);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(amax);
+  if (int rc = launch_pdl(tensor_amax_kernel, ga, stream, x, n, bits)) return rc;
+  return launch_pdl(tensorwise_kernel, gc, stream, x, n, static_cast<const uint32_t*>(bits), q,
+                    scale);
+}
+
+int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint16_t* scale,
+                        int num_sms, cudaStream_t stream) {
+  // Threads per row: enough for one 16-byte chunk each, 32 to 256.
+  int t_log2 = 5;
+  while (t_log2 < 8 && (int64_t{8} << (t_log2 + 1)) <= K) ++t_log2;
+  const int64_t groups = kThreads >> t_log2;
+  const int64_t steps = (M + groups - 1) / groups;
+  const int64_t per_thread = ((K >> 3) + (1 << t_log2) - 1) >> t_log2;   // chunks
+  auto go = [&](auto kernel) {
+    int per = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kThreads, 0) != cudaSuccess ||
+        per < 1)
+      per = 1;
+    const int64_t want = static_cast<int64_t>(num_sms) * per;
+    const int grid = static_cast<int>(steps < want ? steps : want);
+    return launch_pdl(kernel, grid, stream, x, M, K, t_log2, q, scale);
+  };
+  if (per_thread <= 1) return go(rowwise_kernel<1>);
+  if (per_thread <= 2) return go(rowwise_kernel<2>);
+  if (per_thread <= 4) return go(rowwise_kernel<4>);
+  if (per_thread <= 8) return go(rowwise_kernel<8>);
+  return go(rowwise_kernel<0>);
+}
+
+}  // namespace mx

@@ -134,3 +134,16 @@ def test_new_entry_points_reject_bad_arguments(lib):
     assert lib.mx_dequant_blocked(A, 0, 64, A, A, None) == mx.MX_ERR_SHAPE
     assert lib.mx_dequant_blocked(A, 64, 48, A, A, None) == mx.MX_ERR_SHAPE
     assert lib.mx_dequant_blocked(A, 64, 64, A, B, None) == mx.MX_ERR_ALIGN
+
+
+def test_scaled_fp8_entry_points_reject_bad_arguments(lib):
+    import ctypes as C
+    F = C.c_void_p(A)
+    assert lib.mx_cast_tensorwise(None, 64, A, F, F, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_tensorwise(A, 0, A, F, F, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_tensorwise(B, 64, A, F, F, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_tensorwise(A, 64, A, C.c_void_p(A + 2), F, None) == mx.MX_ERR_ALIGN
+    assert lib.mx_cast_rowwise(A, 64, 64, None, A, None) == mx.MX_ERR_NULL
+    assert lib.mx_cast_rowwise(A, 64, 12, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_rowwise(A, 0, 64, A, A, None) == mx.MX_ERR_SHAPE
+    assert lib.mx_cast_rowwise(A, 64, 64, B, A, None) == mx.MX_ERR_ALIGN
