@@ -216,10 +216,12 @@ const char* mx_strerror(int code) {
 int mx_last_cuda_error(void) { return t_last_cuda; }
 
 int mx_watchdog(int clear) {
-  int v = 0;
+  int v = 0, w = 0;
   int rc = mx::read_watchdog(&v, clear != 0);
   if (rc) return cuda_fail(rc);
-  return v;
+  rc = mx::read_scaled_watchdog(&w, clear != 0);
+  if (rc) return cuda_fail(rc);
+  return v | w;
 }
 
 int mx_selftest_watchdog(int64_t wait_ns, void* stream) {

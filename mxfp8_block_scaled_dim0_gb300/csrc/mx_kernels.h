@@ -54,6 +54,7 @@ int launch_group_offsets(const int32_t* offs, int G, int64_t M, int64_t* row_off
 int launch_scales_to_blocked(const uint8_t* s, int64_t R, int64_t C, uint8_t* out,
                              cudaStream_t stream);
 int read_watchdog(int* out, bool clear);
+int read_scaled_watchdog(int* out, bool clear);   // the rowwise kernel's word (mx_scaled.cu)
 int launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace mx

@@ -18,10 +18,11 @@
 // Rowwise ("FP8 linear triton with row-wise scaling" gist,
 // quantize_fp8_rowwise): scale_r = bf16(amax_r / 448), q = e4m3(fp32(x /
 // scale_r)); a zero scale gives signed zeros.  A group of T threads (32 to
-// 256, by K) owns a row: it reduces the row's amax, keeping its part of the
-// row in registers (up to 8 chunks of 8 values per thread, K <= 16384; longer
-// rows are read again, from L2), then divides and converts.  The division is
-// a reciprocal product with one residual correction, exact for these
+// 256, by K) owns a row.  The rows of each step (one to eight) arrive in
+// shared memory by one bulk async copy issued steps ahead (rowwise_bulk_kernel;
+// rows longer than 24576 values are read from global memory twice instead);
+// the group reduces the row's amax, then divides and converts.  The division
+// is a reciprocal product with one residual correction, exact for these
 // operands (row_quot_fast).
 //
 // Exactness against a single rounding: the fp32 product of a bf16 value and
@@ -41,6 +42,12 @@ namespace mx {
 namespace {
 
 constexpr int kThreads = 256;
+// Bulk-staged rowwise: ring bytes per CTA.  Measured on GB300 at 16384^2 (one
+// 32 KB row per stage): 64 KB (2 stages, 3 CTAs per SM) 138.7 us; 96 KB
+// (2 CTAs per SM) 150.3 us; 128-160 KB (1 CTA per SM) 215.8 us; 512-thread
+// CTAs or a register cap for more resident CTAs were slower too.
+constexpr int64_t kRowRing = 64 * 1024;
+constexpr int64_t kMaxRowStage = 48 * 1024;   // largest stage (rows of one step) it takes
 
 __device__ __forceinline__ float div_rn(float a, float b) {
   float r;
@@ -191,11 +198,8 @@ __device__ __forceinline__ uint16_t row_scale(uint32_t m, uint32_t* red, int g, 
   return sb;
 }
 
-// kHold > 0: each thread keeps its (at most kHold) chunks of the row in
-// registers between the amax reduction and the conversion, so the row is
-// read once.  kHold == 0: rows too long for that are read twice (the second
-// read hits L2).
-template <int kHold>
+// Rows too long for the bulk-staged kernel (stage over kMaxRowStage): the
+// group reads its row twice, the second time from L2.
 __global__ void __launch_bounds__(kThreads) rowwise_kernel(const uint16_t* x, int64_t M,
                                                            int64_t K, int t_log2, uint8_t* q,
                                                            uint16_t* scale) {
@@ -214,54 +218,126 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const uint16_t* x, in
     const uint4* xr = reinterpret_cast<const uint4*>(x + r * K);
     uint2* qr = reinterpret_cast<uint2*>(q + r * K);
     uint32_t m = 0;
-    if (kHold > 0) {
-      uint4 v[kHold > 0 ? kHold : 1];
-#pragma unroll
-      for (int i = 0; i < kHold; ++i) {
-        const int64_t c = tid + static_cast<int64_t>(i) * T;
-        v[i] = live && c < chunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
-        m = max(m, mag_max8(v[i]));
+    if (live) {
+      for (int64_t c = tid; c < chunks; c += 2 * T) {
+        const uint4 a = __ldg(xr + c);
+        uint4 b = make_uint4(0, 0, 0, 0);
+        if (c + T < chunks) b = __ldg(xr + c + T);
+        m = max(m, max(mag_max8(a), mag_max8(b)));
       }
-      const uint16_t sb = row_scale(m, red, g, t_log2);
-      if (!live) continue;
-      const float s = __uint_as_float(static_cast<uint32_t>(sb) << 16);
-      if (tid == 0) scale[r] = sb;
-      const bool fast = s >= FLT_MIN && s <= FLT_MAX;
-      const float rcp = fast ? div_rn(1.0f, s) : 0.0f;
-#pragma unroll
-      for (int i = 0; i < kHold; ++i) {
-        const int64_t c = tid + static_cast<int64_t>(i) * T;
-        if (c >= chunks) break;
-        uint2 o;
-        if (fast) {
-          o.x = row_e4m3x2<true>(v[i].x, s, rcp) | (row_e4m3x2<true>(v[i].y, s, rcp) << 16);
-          o.y = row_e4m3x2<true>(v[i].z, s, rcp) | (row_e4m3x2<true>(v[i].w, s, rcp) << 16);
-        } else {
-          o.x = row_e4m3x2<false>(v[i].x, s, 0.0f) | (row_e4m3x2<false>(v[i].y, s, 0.0f) << 16);
-          o.y = row_e4m3x2<false>(v[i].z, s, 0.0f) | (row_e4m3x2<false>(v[i].w, s, 0.0f) << 16);
-        }
-        qr[c] = o;
-      }
-    } else {
-      if (live) {
-        for (int64_t c = tid; c < chunks; c += 2 * T) {
-          const uint4 a = __ldg(xr + c);
-          uint4 b = make_uint4(0, 0, 0, 0);
-          if (c + T < chunks) b = __ldg(xr + c + T);
-          m = max(m, max(mag_max8(a), mag_max8(b)));
-        }
-      }
-      const uint16_t sb = row_scale(m, red, g, t_log2);
-      if (!live) continue;
-      const float s = __uint_as_float(static_cast<uint32_t>(sb) << 16);
-      if (tid == 0) scale[r] = sb;
-      // Normal finite scales take the reciprocal path; zero, subnormal, Inf
-      // and NaN scales the IEEE division.
-      if (s >= FLT_MIN && s <= FLT_MAX)
-        row_pass2<true>(xr, qr, chunks, tid, T, s, div_rn(1.0f, s));
-      else
-        row_pass2<false>(xr, qr, chunks, tid, T, s, 0.0f);
     }
+    const uint16_t sb = row_scale(m, red, g, t_log2);
+    if (!live) continue;
+    const float s = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+    if (tid == 0) scale[r] = sb;
+    // Normal finite scales take the reciprocal path; zero, subnormal, Inf
+    // and NaN scales the IEEE division.
+    if (s >= FLT_MIN && s <= FLT_MAX)
+      row_pass2<true>(xr, qr, chunks, tid, T, s, div_rn(1.0f, s));
+    else
+      row_pass2<false>(xr, qr, chunks, tid, T, s, 0.0f);
+  }
+}
+
+// Bulk-staged rowwise variant: each step's rows (R = 256 / T consecutive rows,
+// contiguous in memory) arrive in shared memory by one 1D bulk async copy,
+// kS steps ahead, completing on an mbarrier; the threads reduce and convert
+// from shared memory and store q directly.  DRAM latency is hidden by the
+// copies in flight instead of by registers.  Every wait is bounded; on time-out
+// the CTA raises its abort flag, stops, and reports through g_scaled_watchdog.
+__device__ int g_scaled_watchdog = 0;
+
+__global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* x, int64_t M,
+                                                                int64_t K, int t_log2, int stages,
+                                                                uint8_t* q, uint16_t* scale) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint32_t red[kThreads / 32];
+  __shared__ __align__(8) uint64_t full[8];
+  __shared__ int abort_flag;
+  const int T = 1 << t_log2;
+  const int groups = kThreads >> t_log2;
+  const int g = threadIdx.x >> t_log2;
+  const int tid = threadIdx.x & (T - 1);
+  const int64_t chunks = K >> 3;
+  const int64_t row_bytes = K * 2;
+  const int64_t stage_bytes = row_bytes * groups;
+  const int64_t step_rows = static_cast<int64_t>(gridDim.x) * groups;
+  const int64_t n_steps = (M - static_cast<int64_t>(blockIdx.x) * groups + step_rows - 1) / step_rows;
+
+  auto issue = [&](int64_t i) {             // thread 0: step i into its stage
+    const int st = static_cast<int>(i % stages);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * groups + i * step_rows;
+    const int64_t rows = M - r0 < groups ? M - r0 : groups;
+    const uint32_t bytes = static_cast<uint32_t>(rows * row_bytes);
+    mbar_arrive_expect_tx(&full[st], bytes);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(ring + st * stage_bytes)),
+        "l"(reinterpret_cast<uint64_t>(x + r0 * K)), "r"(bytes), "r"(smem_u32(&full[st]))
+        : "memory");
+  };
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < stages; ++st) mbar_init(&full[st], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  int64_t issued = 0;                        // meaningful in thread 0
+  if (threadIdx.x == 0)
+    for (; issued < stages && issued < n_steps; ++issued) issue(issued);
+
+  int64_t i = 0;
+  for (; i < n_steps; ++i) {
+    const int st = static_cast<int>(i % stages);
+    const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1), &abort_flag);
+    if (!__syncthreads_and(ok)) break;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * groups + i * step_rows + g;
+    const bool live = r < M;
+    const uint4* xs = reinterpret_cast<const uint4*>(ring + st * stage_bytes + g * row_bytes);
+    uint32_t m = 0;
+    if (live)
+      for (int64_t c = tid; c < chunks; c += T) m = max(m, mag_max8(xs[c]));
+    const uint16_t sb = row_scale(m, red, g, t_log2);
+    const float sv = __uint_as_float(static_cast<uint32_t>(sb) << 16);
+    if (live) {
+      if (tid == 0) scale[r] = sb;
+      uint2* qr = reinterpret_cast<uint2*>(q + r * K);
+      if (sv >= FLT_MIN && sv <= FLT_MAX) {
+        const float rcp = div_rn(1.0f, sv);
+        for (int64_t c = tid; c < chunks; c += T) {
+          const uint4 a = xs[c];
+          uint2 o;
+          o.x = row_e4m3x2<true>(a.x, sv, rcp) | (row_e4m3x2<true>(a.y, sv, rcp) << 16);
+          o.y = row_e4m3x2<true>(a.z, sv, rcp) | (row_e4m3x2<true>(a.w, sv, rcp) << 16);
+          qr[c] = o;
+        }
+      } else {
+        for (int64_t c = tid; c < chunks; c += T) {
+          const uint4 a = xs[c];
+          uint2 o;
+          o.x = row_e4m3x2<false>(a.x, sv, 0.0f) | (row_e4m3x2<false>(a.y, sv, 0.0f) << 16);
+          o.y = row_e4m3x2<false>(a.z, sv, 0.0f) | (row_e4m3x2<false>(a.w, sv, 0.0f) << 16);
+          qr[c] = o;
+        }
+      }
+    }
+    __syncthreads();                          // every thread is done with this stage
+    if (threadIdx.x == 0 && i + stages < n_steps) issue(issued++);
+  }
+  if (threadIdx.x == 0 && abort_flag) {
+    // Gave up waiting: let the copies still in flight land (bounded) before
+    // the CTA's shared memory is released, then report.
+    for (int64_t j = i; j < issued; ++j) {
+      const int st = static_cast<int>(j % stages);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&full[st], static_cast<uint32_t>((j / stages) & 1)) &&
+             globaltimer_ns() - t0 < 100000000ull) {
+      }
+    }
+    atomicOr(&g_scaled_watchdog, 1);
   }
 }
 
@@ -315,21 +391,55 @@ int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uin
   while (t_log2 < 8 && (int64_t{8} << (t_log2 + 1)) <= K) ++t_log2;
   const int64_t groups = kThreads >> t_log2;
   const int64_t steps = (M + groups - 1) / groups;
-  const int64_t per_thread = ((K >> 3) + (1 << t_log2) - 1) >> t_log2;   // chunks
-  auto go = [&](auto kernel) {
+  const int64_t stage_bytes = groups * K * 2;
+  if (stage_bytes <= kMaxRowStage) {
+    // Bulk-staged: as many stages (2..8) as fit in kRowRing bytes.
+    int stages = static_cast<int>(kRowRing / stage_bytes);
+    stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+    const int smem = static_cast<int>(stages * stage_bytes);
+    static const int attr = [] {
+      return static_cast<int>(cudaFuncSetAttribute(
+          rowwise_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          static_cast<int>(kRowRing > 2 * kMaxRowStage ? kRowRing : 2 * kMaxRowStage)));
+    }();
+    if (attr != 0) return attr;
     int per = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, rowwise_bulk_kernel, kThreads, smem) !=
+            cudaSuccess ||
         per < 1)
       per = 1;
     const int64_t want = static_cast<int64_t>(num_sms) * per;
     const int grid = static_cast<int>(steps < want ? steps : want);
-    return launch_pdl(kernel, grid, stream, x, M, K, t_log2, q, scale);
-  };
-  if (per_thread <= 1) return go(rowwise_kernel<1>);
-  if (per_thread <= 2) return go(rowwise_kernel<2>);
-  if (per_thread <= 4) return go(rowwise_kernel<4>);
-  if (per_thread <= 8) return go(rowwise_kernel<8>);
-  return go(rowwise_kernel<0>);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr_pdl[1];
+    attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_pdl;
+    cfg.numAttrs = 1;
+    return static_cast<int>(
+        cudaLaunchKernelEx(&cfg, rowwise_bulk_kernel, x, M, K, t_log2, stages, q, scale));
+  }
+  static const int per = wave(rowwise_kernel, 1);
+  const int64_t want = static_cast<int64_t>(num_sms) * per;
+  const int grid = static_cast<int>(steps < want ? steps : want);
+  return launch_pdl(rowwise_kernel, grid, stream, x, M, K, t_log2, q, scale);
+}
+
+int read_scaled_watchdog(int* out, bool clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_scaled_watchdog, sizeof(int));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  if (clear && v) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_scaled_watchdog, &z, sizeof(int));
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
+  *out = v;
+  return 0;
 }
 
 }  // namespace mx

@@ -24,8 +24,10 @@ def cuda_lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     mx.library()
+    assert mx.mx_watchdog(clear=True) == 0
     yield
     torch.cuda.synchronize()
+    assert mx.mx_watchdog(clear=True) == 0
 
 
 def to_np(t):
@@ -163,7 +165,7 @@ def test_tensorwise_full_size_sampled():
 
 
 @pytest.mark.parametrize("M,K", [(1, 8), (3, 24), (77, 96), (256, 384), (64, 4128), (1000, 512),
-                                 (5, 16392)])
+                                 (5, 16392), (3, 24584), (2, 40000)])
 def test_rowwise_matches_oracle(M, K):
     t = W.wide(M, K, 3 * M + K, zero_frac=0.02)
     compare_rowwise(W.bf16_bits(t), "%dx%d" % (M, K))
