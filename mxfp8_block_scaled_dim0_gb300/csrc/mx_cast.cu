@@ -414,32 +414,50 @@ __device__ __forceinline__ uint4 staged_chunk(const uint8_t* srow, int sw, int k
 // rows in place onto their aligned chunks (chunk 0 completes the previous
 // tile's partial last chunk from the carried bytes), so that each row is one
 // 16-byte aligned 128-byte TMA box.  The row's raw last 16 bytes become the
-// carried chunk of the next tile.  Rows 32*sw_idx .. +31, eight lanes per row
-// (lane j takes chunk j); every read happens before any write.
+// carried chunk of the next tile.  One lane per q1 row: store warp sw_idx owns
+// staging rows 16*sw_idx .. +15 of both halves (the rows it stores by TMA);
+// each 8-lane phase takes eight consecutive staging rows of one half, whose
+// swizzles differ, so the 16-byte accesses are conflict-free.  The lane loads
+// its extended row [carried chunk | 128 staged bytes] (36 words), shifts it by
+// the uniform byte offset 16 - delta (word offset by two select levels, byte
+// offset by funnel shifts) and writes it back; no lane touches another's row.
 __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta, int sw_idx,
                                               int lane) {
-  const int j = lane & 7;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint4 v[4], last[4];
-#pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int c = 32 * sw_idx + (4 * half + pp) * 4 + (lane >> 3);
-      const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
-      const int sw = (c >> 1) & 7;
-      v[pp] = aligned_chunk(srow, sw, carry + c * 16, j, delta);
-      if (j == 0) last[pp] = staged_chunk(srow, sw, 7);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int c = 32 * sw_idx + (4 * half + pp) * 4 + (lane >> 3);
-      uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
-      const int sw = (c >> 1) & 7;
-      *reinterpret_cast<uint4*>(srow + ((j ^ sw) << 4)) = v[pp];
-      if (j == 0) *reinterpret_cast<uint4*>(carry + c * 16) = last[pp];
-    }
+  const int i = lane & 7, ph = lane >> 3;
+  const int mrow = (2 * sw_idx + (ph >> 1)) * 8 + i;   // staging row, 16*sw_idx .. +15
+  const int h = ph & 1;                                  // even / odd q1 half
+  const int c = 2 * mrow + h;                            // q1 row within the tile
+  uint8_t* srow = q1s + h * kQ1Half + mrow * 128;
+  const int sw = mrow & 7;
+  uint8_t* cslot = carry + c * 16;
+  uint32_t e[36];
+  {
+    const uint4 v = *reinterpret_cast<const uint4*>(cslot);
+    e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
   }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = *reinterpret_cast<const uint4*>(srow + ((k ^ sw) << 4));
+    e[4 + 4 * k] = v.x; e[5 + 4 * k] = v.y; e[6 + 4 * k] = v.z; e[7 + 4 * k] = v.w;
+  }
+  const int s = 16 - delta;                              // 1 .. 15
+  const bool q1b = (s >> 2) & 1, q2b = (s >> 2) & 2;
+  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
+  uint32_t f[35], g[33];
+#pragma unroll
+  for (int t = 0; t < 35; ++t) f[t] = q1b ? e[t + 1] : e[t];
+#pragma unroll
+  for (int t = 0; t < 33; ++t) g[t] = q2b ? f[t + 2] : f[t];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint4 o;
+    o.x = __funnelshift_r(g[4 * k], g[4 * k + 1], r);
+    o.y = __funnelshift_r(g[4 * k + 1], g[4 * k + 2], r);
+    o.z = __funnelshift_r(g[4 * k + 2], g[4 * k + 3], r);
+    o.w = __funnelshift_r(g[4 * k + 3], g[4 * k + 4], r);
+    *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = o;
+  }
+  *reinterpret_cast<uint4*>(cslot) = make_uint4(e[32], e[33], e[34], e[35]);
 }
 
 // Grouped mode, other tiles (strip ends, partial tiles, odd M): store the
