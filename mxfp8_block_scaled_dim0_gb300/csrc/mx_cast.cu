@@ -166,6 +166,27 @@ struct GroupTab {
 
 
 
+// q = a / b, r = a - q * b for non-negative a and positive b, in 32 bits
+// when both fit (always, for tile counts of buffers that fit in memory).
+// Used by the grouped schedule; the 2D and 3D schedules keep the plain
+// division (with 32-bit division and counters the 3D kernel measured 3.6%
+// slower).
+__device__ __forceinline__ int64_t div_tiles(int64_t a, int64_t b, int64_t& r) {
+  if (((a | b) >> 32) == 0) {
+    const uint32_t q = static_cast<uint32_t>(a) / static_cast<uint32_t>(b);
+    r = a - static_cast<int64_t>(q) * b;
+    return q;
+  }
+  const int64_t q = a / b;
+  r = a - q * b;
+  return q;
+}
+
+// Per-role tile counter: 32-bit in the grouped mode (1.6 us faster at
+// 16640 x 5120, G = 4, measured against the 64-bit counter).
+template <int M> struct ItType { using T = int64_t; };
+template <> struct ItType<kModeGrouped> { using T = uint32_t; };
+
 // Tile t of the launch.  2D / 3D modes: row-major over (M tiles, K tiles).
 // Grouped mode: ordered by group, then K tile, then M tile within the group,
 // so that a CTA's contiguous run of tiles walks down one column strip of a
@@ -185,8 +206,8 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, i
     const int64_t tr_g = tab.tr(g);
     const int64_t n_tg = tab.tr(g + 1) - tr_g;
     const int64_t v = t - tr_g * p.n_kt;
-    const int64_t tk = v / n_tg;
-    const int64_t tm = v - tk * n_tg;             // tile index within the group
+    int64_t tm;                                   // tile index within the group
+    const int64_t tk = div_tiles(v, n_tg, tm);
     const int64_t start = g ? tab.end(g - 1) : 0;
     const int64_t m0 = start + (tm << 7);
     const int64_t left = tab.end(g) - m0;
@@ -627,7 +648,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tmap(&tm_x);
-      int64_t it = 0;
+      typename ItType<kMode>::T it = 0;
       for (int64_t t = first; t < end; t += step, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
@@ -646,7 +667,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       prefetch_tmap(&tm_q1e);
       prefetch_tmap(&tm_q1o);
     }
-    int64_t it = 0;
+    typename ItType<kMode>::T it = 0;
     for (int64_t t = first; t < end; t += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
@@ -717,7 +738,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     __syncwarp();
   } else {
     // compute warps
-    int64_t it = 0;
+    typename ItType<kMode>::T it = 0;
     for (int64_t t = first; t < end; t += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
