@@ -147,15 +147,18 @@ def test_3d_fused_matches_oracle(E, N, K):
 
 def test_3d_fused_expert_workload_sampled():
     """The (16, 8192, 5120) expert weights through the fused 3D launch: q1 and
-    s1 equal the dim1-only launch; sampled rows of q0 and every expert's
-    sampled scale rows against the oracle."""
+    s1 equal the dim1-only launch, q0 and s0 the dim0-only launch; sampled
+    rows of q0 and every third expert's sampled scale rows against the
+    oracle."""
     w = W.make("experts16x8192x5120", device="cuda")["x"]
     E, N, K = w.shape
     q0, s0, q1, s1 = mx.cast_3d_dim0_dim1(w)
     r1, rs1 = mx.cast_3d_dim1(w)
+    r0, rs0 = mx.cast_3d_dim0(w)
     torch.cuda.synchronize()
     assert torch.equal(q1, r1) and torch.equal(s1, rs1)
-    del r1, rs1
+    assert torch.equal(q0, r0) and torch.equal(s0, rs0)
+    del r1, rs1, r0, rs0
     per = mx.mx_blocked_bytes(N, K // 32)
     g = torch.Generator().manual_seed(4)
     for e in range(0, E, 3):
@@ -251,3 +254,38 @@ def test_dequant_full_size_sampled():
     plain = oracle.from_blocked(to_np(s0), M, K // 32)[rows.numpy()]
     want = oracle.dequant_blocked(to_np(q0[rows.cuda()]), oracle.to_blocked(plain))
     assert_bf16_equal(bf16_np(d[rows.cuda()]), want, "dequant rows")
+
+
+def test_cuda_graph_capture_of_the_other_entry_points():
+    """dim0, 3D, dequantisation, tensorwise (memset + two kernels) and rowwise
+    calls captured in one CUDA graph replay to the bytes of direct calls."""
+    x = W.wide(384, 256, 91).cuda()
+    w = W.experts(2, 96, 160, 92).cuda()
+    calls = [
+        (lambda: mx.cast_dim0(x), lambda o: mx.mx_cast_dim0(x, *o)),
+        (lambda: mx.cast_3d_dim0_dim1(w), lambda o: mx.mx_cast_3d_dim0_dim1(w, *o)),
+        (lambda: mx.cast_3d_dim0(w), lambda o: mx.mx_cast_3d_dim0(w, *o)),
+        (lambda: mx.cast_tensorwise(x), lambda o: mx.mx_cast_tensorwise(x, *o)),
+        (lambda: mx.cast_rowwise(x), lambda o: mx.mx_cast_rowwise(x, *o)),
+    ]
+    refs = [make() for make, _ in calls]
+    q0, s0 = refs[0]
+    dq_ref = mx.dequant_blocked(q0, s0)
+    outs = [tuple(torch.empty_like(t) for t in r) for r in refs]
+    dq_out = torch.empty_like(dq_ref)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for (_, call), o in zip(calls, outs):
+            call(o)
+        mx.mx_dequant_blocked(q0, s0, dq_out)
+    for o in outs:
+        for t in o:
+            t.zero_()
+    dq_out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for r, o in zip(refs, outs):
+        for a, b in zip(r, o):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert torch.equal(dq_ref.view(torch.int16), dq_out.view(torch.int16))
