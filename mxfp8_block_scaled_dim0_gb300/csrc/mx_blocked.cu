@@ -100,6 +100,8 @@ constexpr int kBlkPitch = kBlkCols / 4 + 1;         // words per shared row
 __global__ void __launch_bounds__(256) to_blocked_kernel(const uint8_t* __restrict__ s, int64_t R,
                                                         int64_t C, uint8_t* __restrict__ out,
                                                         int64_t n_ct, int vec16) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ uint32_t tile[128 * kBlkPitch];
   const int64_t rb = blockIdx.y;
   const int64_t ct0 = static_cast<int64_t>(blockIdx.x) * (kBlkCols / 4);   // first column tile
@@ -160,8 +162,19 @@ int launch_scales_to_blocked(const uint8_t* s, int64_t R, int64_t C, uint8_t* ou
   dim3 grid(static_cast<unsigned>((n_ct + kBlkCols / 4 - 1) / (kBlkCols / 4)),
             static_cast<unsigned>(n_rb));
   const int vec16 = (C % 16 == 0) && ((reinterpret_cast<uintptr_t>(s) & 15) == 0);
-  to_blocked_kernel<<<grid, 256, 0, stream>>>(s, R, C, out, n_ct, vec16);
-  return static_cast<int>(cudaGetLastError());
+  // Programmatic dependent of the previous work in the stream (waits for it
+  // before any memory access), so its launch overlaps the previous tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, to_blocked_kernel, s, R, C, out, n_ct, vec16));
 }
 
 }  // namespace mx
