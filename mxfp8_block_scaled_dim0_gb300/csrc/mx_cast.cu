@@ -187,37 +187,12 @@ __device__ __forceinline__ int64_t div_tiles(int64_t a, int64_t b, int64_t& r) {
 template <int M> struct ItType { using T = int64_t; };
 template <> struct ItType<kModeGrouped> { using T = uint32_t; };
 
-// Tile t of the launch.  2D / 3D modes: row-major over (M tiles, K tiles).
-// Grouped mode: ordered by group, then K tile, then M tile within the group,
-// so that a CTA's contiguous run of tiles walks down one column strip of a
-// group (this lets q1 rows be written in whole 16-byte chunks, see
-// copy_out_q1).
+// Tile t of the launch in the 2D / 3D modes: row-major over (M tiles, K tiles).
 template <int kMode>
 __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, int64_t t) {
   Tile T;
   T.cont = 0;
-  if (kMode == kModeGrouped) {
-    int lo = 0, hi = p.G;                          // tr(lo)*n_kt <= t < tr(hi)*n_kt
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (tab.tr(mid) * p.n_kt <= t) lo = mid; else hi = mid;
-    }
-    const int g = lo;
-    const int64_t tr_g = tab.tr(g);
-    const int64_t n_tg = tab.tr(g + 1) - tr_g;
-    const int64_t v = t - tr_g * p.n_kt;
-    int64_t tm;                                   // tile index within the group
-    const int64_t tk = div_tiles(v, n_tg, tm);
-    const int64_t start = g ? tab.end(g - 1) : 0;
-    const int64_t m0 = start + (tm << 7);
-    const int64_t left = tab.end(g) - m0;
-    T.m0 = static_cast<int32_t>(m0);
-    T.k0 = static_cast<int32_t>(tk * kTile);
-    T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
-    T.cont = (tm > 0 ? 1 : 0) | (tm + 1 < n_tg ? 2 : 0);
-    T.s0_dst = p.s0 + ((tr_g + tm) * p.n_kt + tk) * kScaleTile;
-    T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (tr_g * 4) + (tk * n_tg + tm) * kScaleTile;
-  } else {
+  {
     const int32_t tm = static_cast<int32_t>(t / p.n_kt);
     const int32_t tk = static_cast<int32_t>(t - static_cast<int64_t>(tm) * p.n_kt);
     T.m0 = tm * kTile;
@@ -242,6 +217,71 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, i
     }
   }
   return T;
+}
+
+// Grouped mode: tiles are ordered by group, then K tile, then M tile within
+// the group, so that a CTA's contiguous run of tiles walks down one column
+// strip of a group (this lets q1 rows be written in whole 16-byte chunks, see
+// copy_out_q1).  Every role walks its run in order, so it keeps a cursor
+// (group, K tile, M tile) that advances one tile at a time: one search of the
+// group table per run instead of a search and a division per tile (the search
+// alone cost about 2 us per doubling of the group count at 16640 x 5120).
+struct GroupCursor {
+  int g;
+  int64_t tr_g, n_tg, tk, tm, start, end;
+
+  __device__ __forceinline__ void set_group(const GroupTab& tab, int gi) {
+    g = gi;
+    tr_g = tab.tr(gi);
+    n_tg = tab.tr(gi + 1) - tr_g;
+    start = gi ? tab.end(gi - 1) : 0;
+    end = tab.end(gi);
+  }
+  __device__ __forceinline__ void init(const Params& p, const GroupTab& tab, int64_t t) {
+    int lo = 0, hi = p.G;                          // tr(lo)*n_kt <= t < tr(hi)*n_kt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tab.tr(mid) * p.n_kt <= t) lo = mid; else hi = mid;
+    }
+    set_group(tab, lo);
+    tk = 0;
+    tm = 0;
+    if (n_tg > 0) tk = div_tiles(t - tr_g * p.n_kt, n_tg, tm);   // else: past the last tile
+  }
+  __device__ __forceinline__ void next(const Params& p, const GroupTab& tab) {
+    if (++tm < n_tg) return;
+    tm = 0;
+    if (++tk < p.n_kt) return;
+    tk = 0;
+    int ng = g + 1;
+    while (ng < p.G && tab.tr(ng + 1) == tab.tr(ng)) ++ng;   // skip empty groups
+    if (ng < p.G) set_group(tab, ng);
+  }
+  __device__ __forceinline__ Tile tile(const Params& p) const {
+    Tile T;
+    const int64_t m0 = start + (tm << 7);
+    const int64_t left = end - m0;
+    T.m0 = static_cast<int32_t>(m0);
+    T.k0 = static_cast<int32_t>(tk * kTile);
+    T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
+    T.cont = (tm > 0 ? 1 : 0) | (tm + 1 < n_tg ? 2 : 0);
+    T.s0_dst = p.s0 + ((tr_g + tm) * p.n_kt + tk) * kScaleTile;
+    T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (tr_g * 4) + (tk * n_tg + tm) * kScaleTile;
+    return T;
+  }
+};
+
+// The tile a role processes at run position t: from the cursor (advanced
+// past it) in the grouped mode, from t otherwise.
+template <int kMode>
+__device__ __forceinline__ Tile role_tile(const Params& p, const GroupTab& tab, int64_t t,
+                                          GroupCursor& cur) {
+  if (kMode == kModeGrouped) {
+    const Tile T = cur.tile(p);
+    cur.next(p, tab);
+    return T;
+  }
+  return get_tile<kMode>(p, tab, t);
 }
 
 // ---- compute units ----------------------------------------------------------
@@ -649,11 +689,13 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     if (lane == 0) {
       prefetch_tmap(&tm_x);
       typename ItType<kMode>::T it = 0;
+      GroupCursor cur;
+      if (kMode == kModeGrouped) cur.init(p, tab, first);
       for (int64_t t = first; t < end; t += step, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
-        const Tile T = get_tile<kMode>(p, tab, t);
+        const Tile T = role_tile<kMode>(p, tab, t, cur);
         uint8_t* dst = smem + kOffIn + s * kInBytes;
         mbar_arrive_expect_tx(&full[s], kInBytes);
         tma_load_2d(dst, &tm_x, T.k0, T.m0, &full[s]);
@@ -668,12 +710,14 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       prefetch_tmap(&tm_q1o);
     }
     typename ItType<kMode>::T it = 0;
+      GroupCursor cur;
+      if (kMode == kModeGrouped) cur.init(p, tab, first);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
       const bool ok = mbar_wait(&sfull[o], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const Tile T = get_tile<kMode>(p, tab, t);
+      const Tile T = role_tile<kMode>(p, tab, t, cur);
       uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
       if (kMode == kModeGrouped) {
         // Grouped: store warp sw owns rows 16*sw .. 16*sw+15 of each q1 half.
@@ -739,6 +783,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   } else {
     // compute warps
     typename ItType<kMode>::T it = 0;
+      GroupCursor cur;
+      if (kMode == kModeGrouped) cur.init(p, tab, first);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
@@ -748,7 +794,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       ok = ok && mbar_wait(&sempty[o], oph ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
 
-      const Tile T = get_tile<kMode>(p, tab, t);
+      const Tile T = role_tile<kMode>(p, tab, t, cur);
       const uint8_t* in = smem + kOffIn + s * kInBytes;
       uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
       uint8_t* sc1 = smem + kOffS1 + o * kScaleTile;
