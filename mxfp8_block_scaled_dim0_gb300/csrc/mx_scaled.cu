@@ -159,14 +159,16 @@ __device__ __forceinline__ float row_quot(float v, float s) {
 // operands carry 8-bit significands, so an inexact quotient lies at least
 // 2^-33 (relative) from every fp32 rounding boundary, far outside the ~2^-46
 // error of the corrected quotient: the result is the correctly rounded fp32
-// quotient, exact ones included.  The sign is taken from v so that -0 stays
-// -0 (the residual of a zero is +0).
+// quotient, exact ones included.  The residual is formed as q1*s - v and
+// negated inside the second FMA, so that a zero keeps its sign: for v = -0,
+// q1 = -0, q1*s - v = +0 and -(+0)*r + (-0) = -0 (for v = +0 the same steps
+// give +0), with no separate sign fix-up.
 __device__ __forceinline__ float row_quot_fast(float v, float s, float r) {
   const float q1 = mul_rn(v, r);
   float rem, q2;
-  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(rem) : "f"(-q1), "f"(s), "f"(v));
-  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(q2) : "f"(rem), "f"(r), "f"(q1));
-  return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) | (__float_as_uint(v) & 0x80000000u));
+  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(rem) : "f"(q1), "f"(s), "f"(-v));
+  asm("fma.rn.f32 %0, %1, %2, %3;" : "=f"(q2) : "f"(-rem), "f"(r), "f"(q1));
+  return q2;
 }
 
 template <bool kFast>
