@@ -8,10 +8,12 @@
 //   amax  = max |x|; scale = fp32(448 / amax) (amax = 0 -> 1, overflow ->
 //   the largest finite fp32); q = e4m3(fp32(x * scale)), nearest even,
 //   saturated.
-//   tensor_amax_kernel  one wave of CTAs, 16-byte loads, integer max of the
-//                       bf16 magnitude bits (NaN patterns order above Inf, so
-//                       a NaN anywhere makes the amax NaN), one atomicMax per
-//                       CTA into the caller's amax word (cleared first)
+//   tensor_amax_kernel  one wave of CTAs, 16-byte loads, a running bf16x2
+//                       magnitude maximum (max.NaN.xorsign.abs, so a NaN
+//                       anywhere makes the amax NaN), one integer atomicMax
+//                       per CTA on the fp32 bits into the caller's amax word
+//                       (cleared first; non-negative floats order like their
+//                       bit patterns)
 //   tensorwise_kernel   programmatic dependent of the amax kernel; walks the
 //                       tensor from the end, so the part of x still in L2 from
 //                       the amax pass is read first
@@ -62,11 +64,16 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return r;
 }
 
-// Largest bf16 magnitude among the eight values of a 16-byte chunk.
-__device__ __forceinline__ uint32_t mag_max8(uint4 v) {
-  const uint32_t m = 0x7FFF7FFFu;
-  const uint32_t a = __vmaxu2(__vmaxu2(v.x & m, v.y & m), __vmaxu2(v.z & m, v.w & m));
-  return max(a & 0xFFFFu, a >> 16);
+// Running bf16x2 magnitude maximum: acc takes the larger |value| of the eight
+// values of a 16-byte chunk in each half (max.NaN.xorsign.abs.bf16x2: a NaN
+// anywhere propagates; the sign bit of the result is not used).
+__device__ __forceinline__ uint32_t absmax8(uint32_t acc, uint4 v) {
+  return absmax2(acc, absmax2(absmax2(v.x, v.y), absmax2(v.z, v.w)));
+}
+
+// Largest bf16 magnitude (bits, 15 of them) held in a bf16x2 accumulator.
+__device__ __forceinline__ uint32_t mag_of(uint32_t acc) {
+  return max(acc & 0x7FFFu, (acc >> 16) & 0x7FFFu);
 }
 
 __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
@@ -99,8 +106,9 @@ __global__ void __launch_bounds__(kThreads) tensor_amax_kernel(const uint16_t* x
       v[u] = c + u * stride < chunks ? __ldg(reinterpret_cast<const uint4*>(x) + c + u * stride)
                                      : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int u = 0; u < kU; ++u) m = max(m, mag_max8(v[u]));
+    for (int u = 0; u < kU; ++u) m = absmax8(m, v[u]);
   }
+  m = mag_of(m);
   if (blockIdx.x == 0 && threadIdx.x == 0)
     for (int64_t i = chunks << 3; i < n; ++i) m = max(m, static_cast<uint32_t>(x[i] & 0x7FFFu));
   m = block_max(m, red);
@@ -230,10 +238,10 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const uint16_t* x, in
         const uint4 a = __ldg(xr + c);
         uint4 b = make_uint4(0, 0, 0, 0);
         if (c + T < chunks) b = __ldg(xr + c + T);
-        m = max(m, max(mag_max8(a), mag_max8(b)));
+        m = absmax8(absmax8(m, a), b);
       }
     }
-    const uint16_t sb = row_scale(m, red, g, t_log2);
+    const uint16_t sb = row_scale(mag_of(m), red, g, t_log2);
     if (!live) continue;
     const float s = __uint_as_float(static_cast<uint32_t>(sb) << 16);
     if (tid == 0) scale[r] = sb;
@@ -306,8 +314,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
     const uint4* xs = reinterpret_cast<const uint4*>(ring + st * stage_bytes + g * row_bytes);
     uint32_t m = 0;
     if (live)
-      for (int64_t c = tid; c < chunks; c += T) m = max(m, mag_max8(xs[c]));
-    const uint16_t sb = row_scale(m, red, g, t_log2);
+      for (int64_t c = tid; c < chunks; c += T) m = absmax8(m, xs[c]);
+    const uint16_t sb = row_scale(mag_of(m), red, g, t_log2);
     const float sv = __uint_as_float(static_cast<uint32_t>(sb) << 16);
     if (live) {
       if (tid == 0) scale[r] = sb;
