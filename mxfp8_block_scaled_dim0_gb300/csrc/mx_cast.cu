@@ -873,14 +873,16 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
 namespace {
 
 int set_smem(const void* fn) {
-  // Attribute set once per process and kernel; cheap to repeat but avoided.
+  // Set once per device and kernel (DeviceCache); cheap to repeat but avoided.
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   return e == cudaSuccess ? 0 : static_cast<int>(e);
 }
 
 template <int kMode>
 int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t stream) {
-  static int attr_rc = set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>));
+  static DeviceCache smem_attr;
+  const int attr_rc =
+      smem_attr.get([] { return set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>)); });
   if (attr_rc != 0) return attr_rc;
   // Launched as a programmatic dependent of the previous work in the stream:
   // when that is a cast kernel (which triggers its dependents early), this

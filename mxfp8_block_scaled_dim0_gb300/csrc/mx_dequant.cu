@@ -162,14 +162,15 @@ int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t
   if (p.n_tiles > 0xFFFFFFFFll - 2ll * 65536 * 1024) return static_cast<int>(cudaErrorInvalidValue);
   // One wave of resident CTAs (as many per SM as registers allow) striding
   // over the tiles together.
-  static int per_sm = [] {
+  static DeviceCache occ;
+  const int per_sm = occ.get([] {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dequant_blocked_kernel, kDqThreads, 0) !=
             cudaSuccess ||
         n < 1)
       n = 1;
     return n;
-  }();
+  });
   const int64_t want = static_cast<int64_t>(num_sms) * per_sm;
   const int grid = static_cast<int>(p.n_tiles < want ? p.n_tiles : want);
   if (grid <= 0) return 0;

@@ -6,7 +6,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace mx {
+
+// Host-side value computed once per device and kept for the process: kernel
+// attributes (cudaFuncSetAttribute acts on the current device) and occupancy.
+// Two threads that race on the first call both compute the same value.
+class DeviceCache {
+ public:
+  static constexpr int kMaxDevices = 64;
+  static constexpr int kUnset = -2147483647 - 1;
+  DeviceCache() {
+    for (auto& x : v_) x.store(kUnset, std::memory_order_relaxed);
+  }
+  template <typename F>
+  int get(F f) {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return f();
+    int x = v_[d].load(std::memory_order_acquire);
+    if (x == kUnset) {
+      x = f();
+      v_[d].store(x, std::memory_order_release);
+    }
+    return x;
+  }
+
+ private:
+  std::atomic<int> v_[kMaxDevices];
+};
 
 // TMA descriptors of one cast call: x (bf16, two 64-column halves per tile,
 // 128B swizzle) and the even / odd rows of q1 (boxes of 128 bytes x 64 rows,

@@ -384,8 +384,9 @@ int wave(K kernel, int num_sms) {
 
 int launch_cast_tensorwise(const uint16_t* x, int64_t n, uint8_t* q, float* scale, float* amax,
                            int num_sms, cudaStream_t stream) {
-  static const int per_amax = wave(tensor_amax_kernel, 1);
-  static const int per_cast = wave(tensorwise_kernel, 1);
+  static DeviceCache occ_amax, occ_cast;
+  const int per_amax = occ_amax.get([] { return wave(tensor_amax_kernel, 1); });
+  const int per_cast = occ_cast.get([] { return wave(tensorwise_kernel, 1); });
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
   if (e != cudaSuccess) return static_cast<int>(e);
   const int64_t chunks = (n >> 3) > 0 ? (n >> 3) : 1;
@@ -412,11 +413,12 @@ int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uin
     int stages = static_cast<int>(kRowRing / stage_bytes);
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
     const int smem = static_cast<int>(stages * stage_bytes);
-    static const int attr = [] {
+    static DeviceCache attr_cache;
+    const int attr = attr_cache.get([] {
       return static_cast<int>(cudaFuncSetAttribute(
           rowwise_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
           static_cast<int>(kRowRing > 2 * kMaxRowStage ? kRowRing : 2 * kMaxRowStage)));
-    }();
+    });
     if (attr != 0) return attr;
     int per = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, rowwise_bulk_kernel, kThreads, smem) !=
@@ -438,7 +440,8 @@ int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uin
     return static_cast<int>(
         cudaLaunchKernelEx(&cfg, rowwise_bulk_kernel, x, M, K, t_log2, stages, q, scale));
   }
-  static const int per = wave(rowwise_kernel, 1);
+  static DeviceCache occ;
+  const int per = occ.get([] { return wave(rowwise_kernel, 1); });
   const int64_t want = static_cast<int64_t>(num_sms) * per;
   const int grid = static_cast<int>(steps < want ? steps : want);
   return launch_pdl(rowwise_kernel, grid, stream, x, M, K, t_log2, q, scale);
