@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused MXFP8 dim0+dim1 cast HBM GB/s and fraction of GB300 HBM peak (1 GPU)"
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e nominal, as the pages quote it
 WORKLOAD = "square16384_weight"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["mxfp8_block_scaled_dim0_gb300/csrc/mx_cast.cu",
@@ -528,6 +529,8 @@ def run_gpu(args):
                          "launch_samples": len(per_launch),
                          "timing": "cuda graph replay" if graph is not None else "stream launches"},
             "frac_of_peak": value / ws / peak,
+            # the pages' nominal HBM figure (8 TB/s), beside the measured copy peak
+            "frac_of_nominal": {"value": value / ws / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": R.launches * args.steps,
