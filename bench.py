@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused MXFP8 dim0+dim1 cast HBM GB/s and fraction of GB300 HBM peak (1 GPU)"
-NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e nominal, as the pages quote it
+NOMINAL_HBM_GBS = 8000.0   # nominal HBM bandwidth, the peak figure pytorch/ao PR #2990's perf analysis uses
 WORKLOAD = "square16384_weight"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["mxfp8_block_scaled_dim0_gb300/csrc/mx_cast.cu",
