@@ -428,49 +428,6 @@ __device__ __forceinline__ void store_partial(uint8_t* g, const uint4& v, int lo
   }
 }
 
-// Grouped mode, q1 rows.  A tile's q1 row segment (its 128 staged bytes)
-// starts `delta` bytes into a 16-byte chunk of q1 (group starts are not
-// aligned).  Chunk j (0..8) of the segment's aligned chunks holds bytes
-// [16j - delta, 16j - delta + 16) of the segment; bytes before 0 are the
-// previous tile's last bytes.  Those come from `cslot`, which holds the
-// previous tile's raw last 16 bytes (its carried chunk), so chunk j is bytes
-// [16 - delta, 32 - delta) of the 32-byte window (a, b) = (extended chunk j,
-// extended chunk j + 1) of the extended row [cslot | staged row].  Two
-// conflict-free 16-byte loads; the uniform word offset (16 - delta) / 4 is
-// applied with three levels of selects, the byte offset with funnel shifts.
-__device__ __forceinline__ uint4 aligned_chunk(const uint8_t* srow, int sw, const uint8_t* cslot,
-                                               int j, int delta) {
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  const uint4 a = j == 0 ? *reinterpret_cast<const uint4*>(cslot)
-                         : *reinterpret_cast<const uint4*>(srow + (((j - 1) ^ sw) << 4));
-  const uint4 b = j <= 7 ? *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4)) : zero;
-  const int s = 16 - delta;                          // 1 .. 16
-  const int q = s >> 2;                              // word offset 0 .. 4
-  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
-  // w[i] = window word q + i, i = 0..4 (window words 8.. are zero)
-  const uint32_t W0 = a.x, W1 = a.y, W2 = a.z, W3 = a.w, W4 = b.x, W5 = b.y, W6 = b.z, W7 = b.w;
-  const bool q1b = q & 1, q2b = q & 2, q4b = q & 4;
-  // shift by (q & 1)
-  const uint32_t t0 = q1b ? W1 : W0, t1 = q1b ? W2 : W1, t2 = q1b ? W3 : W2, t3 = q1b ? W4 : W3,
-                 t4 = q1b ? W5 : W4, t5 = q1b ? W6 : W5, t6 = q1b ? W7 : W6, t7 = q1b ? 0u : W7;
-  // shift by (q & 2)
-  const uint32_t u0 = q2b ? t2 : t0, u1 = q2b ? t3 : t1, u2 = q2b ? t4 : t2, u3 = q2b ? t5 : t3,
-                 u4 = q2b ? t6 : t4, u5 = q2b ? t7 : t5, u6 = q2b ? 0u : t6, u7 = q2b ? 0u : t7;
-  // shift by (q & 4)
-  const uint32_t x0 = q4b ? u4 : u0, x1 = q4b ? u5 : u1, x2 = q4b ? u6 : u2, x3 = q4b ? u7 : u3,
-                 x4 = q4b ? 0u : u4;
-  uint4 o;
-  o.x = __funnelshift_r(x0, x1, r);
-  o.y = __funnelshift_r(x1, x2, r);
-  o.z = __funnelshift_r(x2, x3, r);
-  o.w = __funnelshift_r(x3, x4, r);
-  return o;
-}
-
-__device__ __forceinline__ uint4 staged_chunk(const uint8_t* srow, int sw, int k) {
-  return *reinterpret_cast<const uint4*>(srow + ((k ^ sw) << 4));
-}
-
 // Grouped mode, whole interior tile of a column strip: rewrite the staged q1
 // rows in place onto their aligned chunks (chunk 0 completes the previous
 // tile's partial last chunk from the carried bytes), so that each row is one
@@ -521,50 +478,77 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
   *reinterpret_cast<uint4*>(cslot) = make_uint4(e[32], e[33], e[34], e[35]);
 }
 
-// Grouped mode, other tiles (strip ends, partial tiles, odd M): store the
-// staged q1 rows (`len` valid bytes each) to q1 row k0 + c, columns m0 ..
-// m0 + len - 1, as the aligned chunks they cover.  Whole chunks take one
-// vector store; a partial chunk (at a strip end, or where the tile above was
-// handled by another CTA) is stored piecewise.  When the tile below follows in
-// this CTA, the last chunk is not stored: it is completed there from the
-// carried raw last 16 bytes of this row.  Rows 32*sw_idx .. +31, eight lanes
-// per row (128 contiguous bytes per row and store); lane 0 of a row also takes
-// the ninth chunk and the carry.
+// Grouped mode, other tiles (strip ends, partial tiles, the first tile of a
+// CTA's run, odd M): store the staged q1 rows (`len` valid bytes each) to q1
+// row k0 + c, columns m0 .. m0 + len - 1, as the aligned chunks they cover.
+// One lane per q1 row, the rows and lane mapping of shift_q1_rows: the lane
+// loads its extended row [carried chunk | 128 staged bytes], forms all nine
+// aligned chunks in registers (the byte offset delta of the row's start in
+// its 16-byte chunk is 0..15 and, when M % 16 != 0, differs by row: three
+// select levels for the word offset, funnel shifts for the bytes) and
+// stores them: whole chunks with one vector store, partial ones (at a strip
+// end, or where the tile above was handled by another CTA) with the fewest
+// aligned 8 / 4 / 2 / 1-byte stores.  When the tile below follows in this
+// CTA, the last chunk is not stored: it is completed there from the carried
+// raw last 16 bytes of this row.
 __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, uint8_t* q1,
                                             int64_t M, int64_t K, int m0, int k0, int len,
                                             bool cont_prev, bool cont_next, int sw_idx, int lane) {
-  const int j = lane & 7;
-#pragma unroll 2
-  for (int pass = 0; pass < 8; ++pass) {
-    const int c = 32 * sw_idx + pass * 4 + (lane >> 3);
-    const int64_t kk = static_cast<int64_t>(k0) + c;
-    if (kk >= K) continue;
-    const int64_t A = kk * M + m0;                   // byte offset of the row segment
-    const int delta = static_cast<int>(A & 15);
-    uint8_t* g = q1 + (A - delta);                   // its first aligned chunk
-    const uint8_t* srow = q1s + (c & 1) * kQ1Half + (c >> 1) * 128;
-    const int sw = (c >> 1) & 7;
-    uint8_t* cslot = carry + c * 16;
-
-    // chunk j: segment bytes [16j - delta, 16j - delta + 16)
-    const int o = 16 * j - delta;
+  const int i = lane & 7, ph = lane >> 3;
+  const int mrow = (2 * sw_idx + (ph >> 1)) * 8 + i;   // staging row, 16*sw_idx .. +15
+  const int h = ph & 1;                                  // even / odd q1 half
+  const int c = 2 * mrow + h;                            // q1 row within the tile
+  const int64_t kk = static_cast<int64_t>(k0) + c;
+  if (kk >= K) return;
+  const uint8_t* srow = q1s + h * kQ1Half + mrow * 128;
+  const int sw = mrow & 7;
+  uint8_t* cslot = carry + c * 16;
+  const int64_t A = kk * M + m0;                         // byte offset of the row segment
+  const int delta = static_cast<int>(A & 15);
+  uint8_t* g = q1 + (A - delta);                         // its first aligned chunk
+  uint32_t e[44];
+  if (cont_prev) {
+    const uint4 v = *reinterpret_cast<const uint4*>(cslot);
+    e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
+  } else {
+    e[0] = e[1] = e[2] = e[3] = 0u;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = *reinterpret_cast<const uint4*>(srow + ((k ^ sw) << 4));
+    e[4 + 4 * k] = v.x; e[5 + 4 * k] = v.y; e[6 + 4 * k] = v.z; e[7 + 4 * k] = v.w;
+  }
+#pragma unroll
+  for (int t = 36; t < 44; ++t) e[t] = 0u;
+  // aligned chunk j = bytes [16j + s, 16j + s + 16) of the extended row
+  const int s = 16 - delta;                              // 1 .. 16
+  const int q = s >> 2;                                  // word offset 0 .. 4
+  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
+  uint32_t f[43], gg[41], w[37];
+#pragma unroll
+  for (int t = 0; t < 43; ++t) f[t] = (q & 1) ? e[t + 1] : e[t];
+#pragma unroll
+  for (int t = 0; t < 41; ++t) gg[t] = (q & 2) ? f[t + 2] : f[t];
+#pragma unroll
+  for (int t = 0; t < 37; ++t) w[t] = (q & 4) ? gg[t + 4] : gg[t];
+#pragma unroll
+  for (int j = 0; j < 9; ++j) {
+    const int o = 16 * j - delta;                        // segment offset of the chunk start
     int b_lo = o < 0 ? -o : 0;
+    if (j == 0 && cont_prev) b_lo = 0;                   // the carried bytes complete it
     const int b_hi = (len - o) < 16 ? (len - o) : 16;
-    if (j == 0 && cont_prev) b_lo = 0;               // the carried bytes complete it
+    if (j == 8 && cont_next) continue;                   // completed by the tile below
     if (b_lo < b_hi) {
-      const uint4 v = aligned_chunk(srow, sw, cslot, j, delta);
+      uint4 v;
+      v.x = __funnelshift_r(w[4 * j], w[4 * j + 1], r);
+      v.y = __funnelshift_r(w[4 * j + 1], w[4 * j + 2], r);
+      v.z = __funnelshift_r(w[4 * j + 2], w[4 * j + 3], r);
+      v.w = __funnelshift_r(w[4 * j + 3], w[4 * j + 4], r);
       if (b_lo == 0 && b_hi == 16) *reinterpret_cast<uint4*>(g + 16 * j) = v;
       else store_partial(g + 16 * j, v, b_lo, b_hi);
     }
-    if (j == 0) {
-      // chunk 8: the segment's last `delta` bytes when it is a whole 128 bytes
-      const int o8 = 128 - delta;
-      const int hi8 = (len - o8) < 16 ? (len - o8) : 16;
-      if (hi8 > 0 && !cont_next)
-        store_partial(g + 128, aligned_chunk(srow, sw, cslot, 8, delta), 0, hi8);
-      if (cont_next) *reinterpret_cast<uint4*>(cslot) = staged_chunk(srow, sw, 7);
-    }
   }
+  if (cont_next) *reinterpret_cast<uint4*>(cslot) = make_uint4(e[32], e[33], e[34], e[35]);
 }
 
 // ---- the kernel -------------------------------------------------------------
