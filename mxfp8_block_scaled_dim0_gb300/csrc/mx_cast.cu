@@ -26,8 +26,12 @@
 //   warp 9     storer: TMA stores of the staged q1 tile, bulk copy of the
 //              dim0 scale tile, and the dim1 scale tile (staged in plain
 //              order, transposed to the blocked order on the way out);
-//              grouped mode: warps 9-12, which also copy q1 out with plain
-//              stores (group starts are not 16-byte aligned)
+//              grouped mode: warps 9-12, one lane per q1 row, which first
+//              shift misaligned rows onto 16-byte chunks in place (group
+//              starts are not 16-byte aligned) or copy strip edges out with
+//              plain stores
+// Modes (template kMode): fused 2D, dim0 only, dim1 only, the 3D per-expert
+// forms of the three, and grouped-M; see the Mode enum.
 // The depths were chosen by measurement on GB300: few input stages and many
 // output staging buffers.  More loads in flight (4-5 stages) slowed the
 // kernel by ~12%: outstanding writes, not reads, limit the mixed stream.
@@ -694,8 +698,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       prefetch_tmap(&tm_q1o);
     }
     typename ItType<kMode>::T it = 0;
-      GroupCursor cur;
-      if (kMode == kModeGrouped) cur.init(p, tab, first);
+    GroupCursor cur;
+    if (kMode == kModeGrouped) cur.init(p, tab, first);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
@@ -767,8 +771,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   } else {
     // compute warps
     typename ItType<kMode>::T it = 0;
-      GroupCursor cur;
-      if (kMode == kModeGrouped) cur.init(p, tab, first);
+    GroupCursor cur;
+    if (kMode == kModeGrouped) cur.init(p, tab, first);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
