@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -49,11 +50,20 @@ def algorithmic_bytes(M, K):
     return 2 * M * K + M * K + M * K + blk(M, K // 32) + blk(K, M // 32)
 
 
+def _code_tokens(text):
+    """Source text without comments and with whitespace collapsed, so that
+    edits to comments or layout do not count as a kernel change."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash():
+    """Hash of the fused kernel's code (comments and whitespace ignored)."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -89,3 +89,12 @@ def test_traffic_is_null_for_other_kernel_code(tmp_path, monkeypatch):
     f.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_full_launch: 123\n"
                  % bench.kernel_source_hash())
     assert bench.measured_traffic() == 123.0
+
+
+def test_kernel_hash_ignores_comments_and_layout():
+    import bench
+    a = "int f(int x) {\n  return x + 1;  // one more\n}\n"
+    b = "/* header */\nint f(int x) { return x + 1; }\n"
+    c = "int f(int x) { return x + 2; }\n"
+    assert bench._code_tokens(a) == bench._code_tokens(b)
+    assert bench._code_tokens(a) != bench._code_tokens(c)
