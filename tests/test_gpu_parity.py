@@ -286,6 +286,7 @@ GROUP_CASES = [
     (512, 256, [128, 384, 384, 512]),          # multiples of 128
     (1000, 384, [0, 0, 333, 334, 999, 1000]),  # empty leading groups, size-1 groups
     (2080, 544, [17, 400, 1111, 2080]),
+    (4224, 640, [0, 1000, 1000, 2999, 4224, 4224]),   # empty first, middle and last groups
 ]
 
 
