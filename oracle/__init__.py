@@ -25,51 +25,54 @@ from . import build as _build
 _lib = None
 
 
+def _configure(lib):
+    """Declare the argument and result types of every oracle entry point."""
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_double.restype = ctypes.c_double
+    lib.oracle_e4m3_rne_sat.argtypes = [ctypes.c_double]
+    lib.oracle_e4m3_rne_sat.restype = ctypes.c_uint8
+    lib.oracle_e4m3_rne_sat_array.argtypes = [P, I64, P]
+    lib.oracle_e4m3_rne_sat_array.restype = None
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_block_scale.argtypes = [P, ctypes.c_int]
+    lib.oracle_block_scale.restype = ctypes.c_uint8
+    lib.oracle_cast_dim0.argtypes = [P, I64, I64, P, P]
+    lib.oracle_cast_dim0.restype = None
+    lib.oracle_cast_dim1.argtypes = [P, I64, I64, P, P]
+    lib.oracle_cast_dim1.restype = None
+    lib.oracle_blocked_bytes.argtypes = [I64, I64]
+    lib.oracle_blocked_bytes.restype = I64
+    lib.oracle_to_blocked.argtypes = [P, I64, I64, P]
+    lib.oracle_to_blocked.restype = None
+    lib.oracle_from_blocked.argtypes = [P, I64, I64, P]
+    lib.oracle_from_blocked.restype = None
+    lib.oracle_cast_dim0_dim1_blocked.argtypes = [P, I64, I64, P, P, P, P]
+    lib.oracle_cast_dim0_dim1_blocked.restype = ctypes.c_int
+    lib.oracle_cast_grouped_m.argtypes = [P, I64, I64, P, ctypes.c_int,
+                                          P, P, P, P, P, P]
+    lib.oracle_cast_grouped_m.restype = ctypes.c_int
+    lib.oracle_cast_3d_dim1.argtypes = [P, I64, I64, I64, P, P]
+    lib.oracle_cast_3d_dim1.restype = ctypes.c_int
+    lib.oracle_cast_3d_dim0.argtypes = [P, I64, I64, I64, P, P]
+    lib.oracle_cast_3d_dim0.restype = ctypes.c_int
+    lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+    lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_dequant_blocked.argtypes = [P, I64, I64, P, P]
+    lib.oracle_dequant_blocked.restype = ctypes.c_int
+    lib.oracle_cast_tensorwise.argtypes = [P, I64, P, P, P]
+    lib.oracle_cast_tensorwise.restype = None
+    lib.oracle_cast_rowwise.argtypes = [P, I64, I64, P, P]
+    lib.oracle_cast_rowwise.restype = None
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
-        path = _build.build()
-        lib = ctypes.CDLL(path)
-        P = ctypes.c_void_p
-        I64 = ctypes.c_int64
-        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
-        lib.oracle_bf16_to_double.restype = ctypes.c_double
-        lib.oracle_e4m3_rne_sat.argtypes = [ctypes.c_double]
-        lib.oracle_e4m3_rne_sat.restype = ctypes.c_uint8
-        lib.oracle_e4m3_rne_sat_array.argtypes = [P, I64, P]
-        lib.oracle_e4m3_rne_sat_array.restype = None
-        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
-        lib.oracle_e4m3_to_double.restype = ctypes.c_double
-        lib.oracle_block_scale.argtypes = [P, ctypes.c_int]
-        lib.oracle_block_scale.restype = ctypes.c_uint8
-        lib.oracle_cast_dim0.argtypes = [P, I64, I64, P, P]
-        lib.oracle_cast_dim0.restype = None
-        lib.oracle_cast_dim1.argtypes = [P, I64, I64, P, P]
-        lib.oracle_cast_dim1.restype = None
-        lib.oracle_blocked_bytes.argtypes = [I64, I64]
-        lib.oracle_blocked_bytes.restype = I64
-        lib.oracle_to_blocked.argtypes = [P, I64, I64, P]
-        lib.oracle_to_blocked.restype = None
-        lib.oracle_from_blocked.argtypes = [P, I64, I64, P]
-        lib.oracle_from_blocked.restype = None
-        lib.oracle_cast_dim0_dim1_blocked.argtypes = [P, I64, I64, P, P, P, P]
-        lib.oracle_cast_dim0_dim1_blocked.restype = ctypes.c_int
-        lib.oracle_cast_grouped_m.argtypes = [P, I64, I64, P, ctypes.c_int,
-                                              P, P, P, P, P, P]
-        lib.oracle_cast_grouped_m.restype = ctypes.c_int
-        lib.oracle_cast_3d_dim1.argtypes = [P, I64, I64, I64, P, P]
-        lib.oracle_cast_3d_dim1.restype = ctypes.c_int
-        lib.oracle_cast_3d_dim0.argtypes = [P, I64, I64, I64, P, P]
-        lib.oracle_cast_3d_dim0.restype = ctypes.c_int
-        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
-        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
-        lib.oracle_dequant_blocked.argtypes = [P, I64, I64, P, P]
-        lib.oracle_dequant_blocked.restype = ctypes.c_int
-        lib.oracle_cast_tensorwise.argtypes = [P, I64, P, P, P]
-        lib.oracle_cast_tensorwise.restype = None
-        lib.oracle_cast_rowwise.argtypes = [P, I64, I64, P, P]
-        lib.oracle_cast_rowwise.restype = None
-        _lib = lib
+        _lib = _configure(ctypes.CDLL(_build.build()))
     return _lib
 
 

@@ -549,3 +549,21 @@ def test_tensorwise_degenerate_scales():
     # all zero -> scale 1
     q, scale, amax = oracle.cast_tensorwise(np.zeros(8, np.uint16))
     assert scale == 1.0 and amax == 0.0 and not q.any()
+
+
+@pytest.mark.parametrize("amax", [3.0, 13.0, 100.0, 0.1875])
+def test_tensorwise_every_element_under_inexact_scales(amax):
+    """Every finite bf16 value of magnitude up to amax, in one tensor whose
+    amax is amax, against the float32 route.  448 / amax is inexact in fp32
+    for these; with amax = 13 some products land differently on the e4m3 grid
+    when the scale is not rounded to fp32 first (the pages' arithmetic rounds
+    it), so the rounding step is pinned."""
+    v = np_bf16_values(FINITE_BF16).astype(np.float32)
+    bits = FINITE_BF16[np.abs(v) <= np.float32(amax)]
+    a_bits = np.float32(amax).view(np.uint32) >> 16
+    x = np.concatenate([np.array([a_bits], np.uint16), bits])
+    q, scale, oamax = oracle.cast_tensorwise(x)
+    xv = np_bf16_values(x).astype(np.float32)
+    s = np.float32(448.0) / np.float32(amax)
+    assert oamax == np.float32(amax) and scale == s
+    assert np.array_equal(q, _e4m3_lib(xv * s))
