@@ -16,6 +16,10 @@
  *     detected on the host before anything is enqueued (outputs untouched).
  *     MX_ERR_CUDA means a CUDA call failed; mx_last_cuda_error() has its code.
  *   - Calls that share an output buffer and run concurrently on the GPU race.
+ *     Inputs and outputs of one call must not overlap.
+ *   - Entry points may be called from several host threads at once: the only
+ *     host state is a per-thread cache of TMA descriptors and per-device
+ *     launch attributes set once.
  *
  * The rule, per 32-element block (OCP Microscaling Formats v1.0 conversion
  * with E4M3 elements and an E8M0 scale):
