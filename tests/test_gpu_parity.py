@@ -400,3 +400,35 @@ def test_cuda_graph_capture_replays_identically():
     torch.cuda.synchronize()
     for a, b in zip(ref + gref, outs + gouts):
         assert torch.equal(a, b)
+
+
+def test_concurrent_host_threads_and_streams():
+    """Four host threads, each with its own stream (and so its own descriptor
+    cache), cast different inputs twenty times over; every result equals the
+    oracle."""
+    import threading
+    xs = [W.wide(512, 384 + 32 * i, 100 + i).cuda() for i in range(4)]
+    results = [None] * 4
+    errors = []
+
+    def work(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(20):
+                    out = mx.cast_dim0_dim1(xs[i], stream=st)
+                st.synchronize()
+            results[i] = tuple(to_np(t) for t in out)
+        except Exception as e:                       # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(4):
+        want = oracle.cast_dim0_dim1_blocked(W.bf16_bits(xs[i].cpu()))
+        for name, g, w in zip(("q0", "s0", "q1", "s1"), results[i], want):
+            assert_bytes_equal(g, w, "thread %d %s" % (i, name))
