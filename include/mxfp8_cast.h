@@ -228,6 +228,22 @@ int mx_last_cuda_error(void);
  * current device, clearing it if `clear` is non-zero, or MX_ERR_CUDA. */
 int mx_watchdog(int clear);
 
+/* Bounds-checked builds (compiled with -DMX_DEBUG_BOUNDS): the number of
+ * global stores the kernels refused because they would have left their
+ * output buffer (each is skipped and counted, never trapped), cleared if
+ * `clear` is non-zero.  The stand-in for a device memory checker.  Returns -1
+ * in a release build (no checks compiled in), MX_ERR_CUDA if the count could
+ * not be read.  Synchronises the current device. */
+int mx_bounds_check(int clear);
+
+/* Diagnostic for bounds-checked builds: one thread tries a 4-byte store just
+ * past an 8-byte span over `buf16` (16 bytes of device memory owned by the
+ * caller, 16-byte aligned); the check refuses it, leaves bytes 8..11
+ * untouched and adds one to the count read by mx_bounds_check().  Returns
+ * MX_OK, MX_ERR_NULL / MX_ERR_ALIGN / MX_ERR_CUDA, or -1 in a release build
+ * (nothing is launched). */
+int mx_selftest_bounds(void* buf16, void* stream);
+
 /* Diagnostic: enqueue one warp that waits, with a limit of `wait_ns`
  * nanoseconds (1e3 .. 1e10), on a barrier that nothing completes.  The wait
  * gives up, sets the watchdog word read by mx_watchdog() and the kernel

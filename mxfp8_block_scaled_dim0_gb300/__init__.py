@@ -32,7 +32,9 @@ ABI_SYMBOLS = (
     "mx_cast_dim0_dim1", "mx_cast_dim0", "mx_cast_dim1", "mx_scales_to_blocked",
     "mx_cast_grouped_m", "mx_cast_3d_dim1", "mx_cast_3d_dim0", "mx_cast_3d_dim0_dim1",
     "mx_dequant_blocked", "mx_blocked_bytes", "mx_grouped_m_scale_bytes", "mx_3d_scale_bytes",
-    "mx_3d_dim0_scale_bytes", "mx_cast_tensorwise", "mx_cast_rowwise", "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
+    "mx_3d_dim0_scale_bytes", "mx_cast_tensorwise", "mx_cast_rowwise", "mx_bounds_check",
+    "mx_selftest_bounds",
+    "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
     "mx_selftest_watchdog",
 )
 
@@ -78,6 +80,8 @@ def _lib():
             "mx_strerror": ([ctypes.c_int], ctypes.c_char_p),
             "mx_last_cuda_error": ([], ctypes.c_int),
             "mx_watchdog": ([ctypes.c_int], ctypes.c_int),
+            "mx_bounds_check": ([ctypes.c_int], ctypes.c_int),
+            "mx_selftest_bounds": ([P, P], ctypes.c_int),
             "mx_selftest_watchdog": ([I64, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
@@ -269,6 +273,25 @@ def mx_selftest_watchdog(wait_ns=50_000_000, stream=None):
     """Run the bounded-wait failure path on the device (no fault): a warp
     waits on a barrier that never completes and gives up after wait_ns."""
     _check(_lib().mx_selftest_watchdog(int(wait_ns), _stream(stream)), "mx_selftest_watchdog")
+
+
+def mx_bounds_check(clear=True):
+    """Stores refused by a bounds-checked build of the library (-1: release
+    build, no checks)."""
+    rc = _lib().mx_bounds_check(1 if clear else 0)
+    if rc < -1:
+        raise MXError(rc, "mx_bounds_check")
+    return rc
+
+
+def mx_selftest_bounds(buf16, stream=None):
+    """Bounds-checked builds: one refused store just past an 8-byte span over
+    buf16 (a 16-byte CUDA tensor); returns 0, or -1 in a release build."""
+    _dev_tensor(buf16, "buf16", 16)
+    rc = _lib().mx_selftest_bounds(_ptr(buf16), _stream(stream))
+    if rc < -1:
+        raise MXError(rc, "mx_selftest_bounds")
+    return rc
 
 
 def mx_watchdog(clear=True):

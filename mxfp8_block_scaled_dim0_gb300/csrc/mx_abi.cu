@@ -224,6 +224,26 @@ int mx_watchdog(int clear) {
   return v | w;
 }
 
+int mx_bounds_check(int clear) {
+  const int parts[4] = {mx::out_of_bounds_cast(clear != 0), mx::out_of_bounds_blocked(clear != 0),
+                        mx::out_of_bounds_dequant(clear != 0), mx::out_of_bounds_scaled(clear != 0)};
+  int sum = 0;
+  for (int v : parts) {
+    if (v == -1) return -1;                     // release build: no checks compiled in
+    if (v < 0) return cuda_fail(static_cast<int>(cudaErrorUnknown));
+    sum += v;
+  }
+  return sum;
+}
+
+int mx_selftest_bounds(void* buf16, void* stream) {
+  if (!buf16) return MX_ERR_NULL;
+  if (!aligned(buf16, 16)) return MX_ERR_ALIGN;
+  const int rc = mx::launch_bounds_selftest(buf16, static_cast<cudaStream_t>(stream));
+  if (rc == -1) return -1;
+  return launch_rc(rc);
+}
+
 int mx_selftest_watchdog(int64_t wait_ns, void* stream) {
   if (wait_ns < 1000 || wait_ns > int64_t{10} * 1000 * 1000 * 1000) return MX_ERR_SHAPE;
   return launch_rc(mx::launch_watchdog_selftest(static_cast<uint64_t>(wait_ns),

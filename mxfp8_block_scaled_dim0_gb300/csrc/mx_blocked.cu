@@ -9,6 +9,7 @@
 //     pytorch/ao PR #2990 "[mxfp8 moe training] add compile support".
 #include <cuda_runtime.h>
 
+#include "mx_common.cuh"
 #include "mx_kernels.h"
 
 namespace mx {
@@ -25,7 +26,8 @@ __global__ void __launch_bounds__(256) group_offsets_kernel(const int32_t* __res
                                                             int G, int64_t M,
                                                             int64_t* __restrict__ row_offs,
                                                             int64_t* __restrict__ col_offs,
-                                                            int32_t* __restrict__ status) {
+                                                            int32_t* __restrict__ status,
+                                                            Span sp_ro, Span sp_co, Span sp_st) {
   __shared__ int64_t warp_sum[32];
   __shared__ int64_t carry_sh;
   __shared__ int bad_sh;
@@ -38,8 +40,8 @@ __global__ void __launch_bounds__(256) group_offsets_kernel(const int32_t* __res
   if (threadIdx.x == 0) {
     carry_sh = 0;
     bad_sh = 0;
-    row_offs[0] = 0;
-    col_offs[0] = 0;
+    if (in_span(sp_ro, row_offs, 8)) row_offs[0] = 0;
+    if (in_span(sp_co, col_offs, 8)) col_offs[0] = 0;
   }
   __syncthreads();
   for (int base = 0; base < G; base += blockDim.x) {
@@ -73,14 +75,14 @@ __global__ void __launch_bounds__(256) group_offsets_kernel(const int32_t* __res
     __syncthreads();
     const int64_t incl = carry + v + (warp ? warp_sum[warp - 1] : 0);
     if (g < G) {
-      row_offs[g + 1] = incl * 128;
-      col_offs[g + 1] = incl * 4;
+      if (in_span(sp_ro, row_offs + g + 1, 8)) row_offs[g + 1] = incl * 128;
+      if (in_span(sp_co, col_offs + g + 1, 8)) col_offs[g + 1] = incl * 4;
     }
     __syncthreads();
     if (threadIdx.x == blockDim.x - 1) carry_sh = incl;
     __syncthreads();
   }
-  if (threadIdx.x == 0) *status = bad_sh ? kErrGroups : 0;
+  if (threadIdx.x == 0 && in_span(sp_st, status, 4)) *status = bad_sh ? kErrGroups : 0;
 }
 
 // Scale matrix s (R x C bytes, row-major) -> blocked layout.  One CTA takes
@@ -99,7 +101,7 @@ constexpr int kBlkPitch = kBlkCols / 4 + 1;         // words per shared row
 
 __global__ void __launch_bounds__(256) to_blocked_kernel(const uint8_t* __restrict__ s, int64_t R,
                                                         int64_t C, uint8_t* __restrict__ out,
-                                                        int64_t n_ct, int vec16) {
+                                                        int64_t n_ct, int vec16, Span sp_out) {
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ uint32_t tile[128 * kBlkPitch];
@@ -140,7 +142,8 @@ __global__ void __launch_bounds__(256) to_blocked_kernel(const uint8_t* __restri
     o.y = tile[(32 + i) * kBlkPitch + j];
     o.z = tile[(64 + i) * kBlkPitch + j];
     o.w = tile[(96 + i) * kBlkPitch + j];
-    *reinterpret_cast<uint4*>(out + (rb * n_ct + ct) * 512 + i * 16) = o;
+    uint8_t* d = out + (rb * n_ct + ct) * 512 + i * 16;
+    if (in_span(sp_out, d, 16)) *reinterpret_cast<uint4*>(d) = o;
   }
 }
 
@@ -150,7 +153,10 @@ int launch_group_offsets(const int32_t* offs, int G, int64_t M, int64_t* row_off
                          int64_t* col_offs, int32_t* status, cudaStream_t stream) {
   // 256 threads: small enough (in registers) to share an SM with a CTA of
   // the cast kernel that follows it as a programmatic dependent.
-  group_offsets_kernel<<<1, 256, 0, stream>>>(offs, G, M, row_offs, col_offs, status);
+  const uint64_t n = 8 * static_cast<uint64_t>(G + 1);
+  group_offsets_kernel<<<1, 256, 0, stream>>>(offs, G, M, row_offs, col_offs, status,
+                                              make_span(row_offs, n), make_span(col_offs, n),
+                                              make_span(status, 4));
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -174,7 +180,34 @@ int launch_scales_to_blocked(const uint8_t* s, int64_t R, int64_t C, uint8_t* ou
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return static_cast<int>(cudaLaunchKernelEx(&cfg, to_blocked_kernel, s, R, C, out, n_ct, vec16));
+  const Span sp_out =
+      make_span(out, static_cast<uint64_t>(n_rb) * 128 * static_cast<uint64_t>(n_ct) * 4);
+  return static_cast<int>(
+      cudaLaunchKernelEx(&cfg, to_blocked_kernel, s, R, C, out, n_ct, vec16, sp_out));
+}
+
+int out_of_bounds_blocked(bool clear) { return read_out_of_bounds(clear); }
+
+#ifdef MX_DEBUG_BOUNDS
+namespace {
+// One thread tries a 4-byte store just past an 8-byte span over the caller's
+// 16-byte buffer: the check must refuse and count it.
+__global__ void bounds_selftest_kernel(uint8_t* buf) {
+  const Span sp = {buf, 8};
+  if (in_span(sp, buf + 8, 4)) *reinterpret_cast<uint32_t*>(buf + 8) = 0xDEADBEEFu;
+}
+}  // namespace
+#endif
+
+int launch_bounds_selftest(void* buf, cudaStream_t stream) {
+#ifdef MX_DEBUG_BOUNDS
+  bounds_selftest_kernel<<<1, 1, 0, stream>>>(static_cast<uint8_t*>(buf));
+  return static_cast<int>(cudaGetLastError());
+#else
+  (void)buf;
+  (void)stream;
+  return -1;
+#endif
 }
 
 }  // namespace mx

@@ -150,6 +150,8 @@ struct Params {
   int32_t k128;             // ceil128(K)
   int32_t q1_tma;           // grouped: q1 rows 16-byte aligned (M % 16 == 0), so
                             // whole 128-byte tiles may leave by TMA
+  // output buffers, for the bounds-checked build's store checks
+  Span sp_q0, sp_q1, sp_s0, sp_s1, sp_ro, sp_co, sp_st;
 };
 
 // Group table of the grouped mode: tr[g] = padded tile-rows before group g
@@ -328,13 +330,15 @@ __device__ __forceinline__ void dim0_half_unit(const uint8_t* in, uint8_t* sc0, 
   o.w = e4m3x4(bf_lo(v1.z), bf_hi(v1.z), bf_lo(v1.w), bf_hi(v1.w), m);
   const int64_t gr = static_cast<int64_t>(m0) + row;
   const int64_t gc = static_cast<int64_t>(k0) + 64 * box + 16 * hq;
-  if (row < rows && gr < M && gc < K) *reinterpret_cast<uint4*>(q0 + gr * K + gc) = o;
+  if (row < rows && gr < M && gc < K && in_span(p.sp_q0, q0 + gr * K + gc, 16))
+    *reinterpret_cast<uint4*>(q0 + gr * K + gc) = o;
   if ((hq & 1) == 0) {
     if (kScatter) {
       if (gr < M && gc < K) {
         const uint32_t e = static_cast<uint32_t>(gr) / static_cast<uint32_t>(p.N);
         const int64_t n = gr - static_cast<int64_t>(e) * p.N;
-        p.s0[e * p.s0_expert_bytes + blocked_offset(n, gc >> 5, p.kb4)] = static_cast<uint8_t>(sbyte);
+        uint8_t* d = p.s0 + e * p.s0_expert_bytes + blocked_offset(n, gc >> 5, p.kb4);
+        if (in_span(p.sp_s0, d, 1)) *d = static_cast<uint8_t>(sbyte);
       }
     } else {
       sc0[blocked_in_tile(row, 2 * box + (hq >> 1))] = static_cast<uint8_t>(row < rows ? sbyte : 0u);
@@ -497,7 +501,8 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
 // raw last 16 bytes of this row.
 __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, uint8_t* q1,
                                             int64_t M, int64_t K, int m0, int k0, int len,
-                                            bool cont_prev, bool cont_next, int sw_idx, int lane) {
+                                            bool cont_prev, bool cont_next, int sw_idx, int lane,
+                                            const Span& sq1) {
   const int i = lane & 7, ph = lane >> 3;
   const int mrow = (2 * sw_idx + (ph >> 1)) * 8 + i;   // staging row, 16*sw_idx .. +15
   const int h = ph & 1;                                  // even / odd q1 half
@@ -548,6 +553,7 @@ __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, 
       v.y = __funnelshift_r(w[4 * j + 1], w[4 * j + 2], r);
       v.z = __funnelshift_r(w[4 * j + 2], w[4 * j + 3], r);
       v.w = __funnelshift_r(w[4 * j + 3], w[4 * j + 4], r);
+      if (!in_span(sq1, g + 16 * j + b_lo, b_hi - b_lo)) continue;
       if (b_lo == 0 && b_hi == 16) *reinterpret_cast<uint4*>(g + 16 * j) = v;
       else store_partial(g + 16 * j, v, b_lo, b_hi);
     }
@@ -628,15 +634,18 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       }
       __syncthreads();
       if (*bad_s) {                           // invalid group offsets: write nothing
-        if (blockIdx.x == 0 && threadIdx.x == 0) *p.status_out = kStatusBadGroups;
+        if (blockIdx.x == 0 && threadIdx.x == 0 && in_span(p.sp_st, p.status_out, 4))
+          *p.status_out = kStatusBadGroups;
         return;
       }
       if (blockIdx.x == 0) {
         for (int g = threadIdx.x; g <= p.G; g += blockDim.x) {
-          p.row_offs_out[g] = static_cast<int64_t>(tr_s[g]) * 128;
-          p.col_offs_out[g] = static_cast<int64_t>(tr_s[g]) * 4;
+          if (in_span(p.sp_ro, p.row_offs_out + g, 8))
+            p.row_offs_out[g] = static_cast<int64_t>(tr_s[g]) * 128;
+          if (in_span(p.sp_co, p.col_offs_out + g, 8))
+            p.col_offs_out[g] = static_cast<int64_t>(tr_s[g]) * 4;
         }
-        if (threadIdx.x == 0) *p.status_out = 0;
+        if (threadIdx.x == 0 && in_span(p.sp_st, p.status_out, 4)) *p.status_out = 0;
       }
       tab.tr_s = tr_s;
       tab.ends_s = ends_s;
@@ -731,14 +740,14 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
           }
         } else {
           copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows, cont_prev,
-                      cont_next, sw, lane);
+                      cont_next, sw, lane, p.sp_q1);
         }
       } else if (kDim1 && lane == 0) {
         tma_store_2d(&tm_q1e, T.m0, T.k0 >> 1, q1s);
         tma_store_2d(&tm_q1o, T.m0, T.k0 >> 1, q1s + kQ1Half);
       }
       if (sw == 0) {
-        if (lane == 0 && kDim0 && T.s0_dst)
+        if (lane == 0 && kDim0 && T.s0_dst && in_span(p.sp_s0, T.s0_dst, kScaleTile))
           bulk_store(T.s0_dst, smem + kOffS0 + o * kScaleTile, kScaleTile);
         if (T.s1_dst) {
           // dim1 scales are staged as [M-block][column]; storage row `lane` of
@@ -754,7 +763,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
                     (static_cast<uint32_t>(nat[256 + c]) << 16) |
                     (static_cast<uint32_t>(nat[384 + c]) << 24);
           }
-          *reinterpret_cast<uint4*>(T.s1_dst + lane * 16) = w;
+          if (in_span(p.sp_s1, T.s1_dst + lane * 16, 16))
+            *reinterpret_cast<uint4*>(T.s1_dst + lane * 16) = w;
         }
       }
       __syncwarp();
@@ -821,7 +831,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int64_t kk = T.k0 + 2 * pcol + h;
-            if (kk < p.K) base[blocked_offset(kk, col, p.nb4)] = static_cast<uint8_t>(sb >> (8 * h));
+            uint8_t* d = base + blocked_offset(kk, col, p.nb4);
+            if (kk < p.K && in_span(p.sp_s1, d, 1)) *d = static_cast<uint8_t>(sb >> (8 * h));
           }
         }
       }
@@ -844,9 +855,11 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kComputeThreads + threadIdx.x;
       const int64_t gstride = static_cast<int64_t>(gridDim.x) * kComputeThreads;
       for (int64_t i = s0_beg / 4 + gtid; i < s0_end / 4; i += gstride)
-        reinterpret_cast<uint32_t*>(p.s0)[i] = 0u;
+        if (in_span(p.sp_s0, reinterpret_cast<uint32_t*>(p.s0) + i, 4))
+          reinterpret_cast<uint32_t*>(p.s0)[i] = 0u;
       for (int64_t i = s1_beg / 4 + gtid; i < s1_end / 4; i += gstride)
-        reinterpret_cast<uint32_t*>(p.s1)[i] = 0u;
+        if (in_span(p.sp_s1, reinterpret_cast<uint32_t*>(p.s1) + i, 4))
+          reinterpret_cast<uint32_t*>(p.s1)[i] = 0u;
     }
   }
 
@@ -892,6 +905,11 @@ int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t strea
 
 }  // namespace
 
+// Bytes of a blocked scale matrix (R x C scales).
+uint64_t blk_bytes(int64_t R, int64_t C) {
+  return static_cast<uint64_t>((R + 127) / 128 * 128) * static_cast<uint64_t>((C + 3) / 4 * 4);
+}
+
 int smem_bytes_cast() { return kSmemBytes; }
 int threads_cast() { return threads_of(kModeFused2D); }
 
@@ -908,6 +926,9 @@ int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s
   prm.n_tiles = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
   prm.s0 = static_cast<uint8_t*>(s0);
   prm.s1 = static_cast<uint8_t*>(s1);
+  prm.sp_q0 = make_span(q0, static_cast<uint64_t>(M) * K);
+  prm.sp_s0 = make_span(s0, blk_bytes(M, K / 32));
+  prm.sp_s1 = make_span(s1, blk_bytes(K, M / 32));
   const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
   if (grid <= 0) return 0;
   if (dim0 && dim1) return launch<kModeFused2D>(maps, prm, grid, stream);
@@ -935,6 +956,9 @@ int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, v
   prm.nb4 = static_cast<int32_t>(((N / 32) + 3) / 4 * 4);
   prm.s1_expert_bytes = ((K + 127) / 128) * 128 * prm.nb4;
   prm.s1_scatter = (N % 128) != 0;
+  prm.sp_q0 = make_span(q0, static_cast<uint64_t>(prm.M) * K);
+  prm.sp_s0 = make_span(s0, static_cast<uint64_t>(E) * prm.s0_expert_bytes);
+  prm.sp_s1 = make_span(s1, static_cast<uint64_t>(E) * prm.s1_expert_bytes);
   const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
   if (grid <= 0) return 0;
   if (dim0 && dim1) return launch<kModeExperts01>(maps, prm, grid, stream);
@@ -963,6 +987,15 @@ int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_
   prm.G = G;
   prm.k128 = static_cast<int32_t>((K + 127) / 128 * 128);
   prm.q1_tma = (M % 16) == 0;
+  prm.sp_q0 = make_span(q0, static_cast<uint64_t>(M) * K);
+  prm.sp_q1 = make_span(q1, static_cast<uint64_t>(M) * K);
+  prm.sp_s0 = make_span(s0, static_cast<uint64_t>(M + 128 * static_cast<int64_t>(G)) *
+                                static_cast<uint64_t>(prm.n_kt) * 4);
+  prm.sp_s1 = make_span(s1, static_cast<uint64_t>(prm.k128) *
+                                static_cast<uint64_t>((M + 31) / 32 + 4 * static_cast<int64_t>(G)));
+  prm.sp_ro = make_span(row_offs, 8 * static_cast<uint64_t>(G + 1));
+  prm.sp_co = make_span(col_offs, 8 * static_cast<uint64_t>(G + 1));
+  prm.sp_st = make_span(status, 4);
   if (G > kMaxSmemGroups) {
     // Large group counts: the padded offsets come from a separate kernel.
     if (int rc = launch_group_offsets(offs, G, M, row_offs, col_offs, status, stream)) return rc;
@@ -993,6 +1026,8 @@ int launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t stream) {
   watchdog_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
   return static_cast<int>(cudaGetLastError());
 }
+
+int out_of_bounds_cast(bool clear) { return read_out_of_bounds(clear); }
 
 int read_watchdog(int* out, bool clear) {
   int v = 0;

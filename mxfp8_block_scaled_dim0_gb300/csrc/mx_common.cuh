@@ -15,6 +15,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace mx {
@@ -204,6 +205,62 @@ __device__ __forceinline__ int blocked_in_tile(int r, int c) {
 __device__ __forceinline__ int64_t blocked_offset(int64_t r, int64_t c, int64_t c4) {
   return ((r >> 7) * (c4 >> 2) + (c >> 2)) * 512 + blocked_in_tile(static_cast<int>(r & 127),
                                                                     static_cast<int>(c & 3));
+}
+
+// ---- bounds-checked builds ------------------------------------------------
+//
+// Built with -DMX_DEBUG_BOUNDS, every global store a kernel issues from its
+// threads is checked against the buffer it belongs to: a store that would
+// leave the buffer is skipped and counted in a device word of the translation
+// unit (read through mx_bounds_check()), never trapped.  The stand-in for a
+// memory checker on machines where none may run.  Release builds compile the
+// checks away.  (TMA tensor stores are bounded by their tensor map's extents
+// in hardware.)
+
+// One output buffer: [base, base + size).
+struct Span {
+  uint8_t* base;
+  uint64_t size;
+};
+
+#ifdef MX_DEBUG_BOUNDS
+static __device__ unsigned int g_out_of_bounds = 0;
+#endif
+
+__device__ __forceinline__ bool in_span(const Span& s, const void* p, uint64_t n) {
+#ifdef MX_DEBUG_BOUNDS
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  const uint64_t b = reinterpret_cast<uint64_t>(s.base);
+  if (s.base != nullptr && a >= b && a - b + n <= s.size) return true;
+  atomicAdd(&g_out_of_bounds, 1u);
+  return false;
+#else
+  (void)s;
+  (void)p;
+  (void)n;
+  return true;
+#endif
+}
+
+inline Span make_span(void* base, uint64_t size) {
+  return Span{static_cast<uint8_t*>(base), size};
+}
+
+// Host: this translation unit's count of refused stores (cleared on request),
+// or -1 in a release build.
+static inline int read_out_of_bounds(bool clear) {
+#ifdef MX_DEBUG_BOUNDS
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_out_of_bounds, sizeof(v)) != cudaSuccess) return -2;
+  if (clear && v) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_out_of_bounds, &z, sizeof(z)) != cudaSuccess) return -2;
+  }
+  return static_cast<int>(v);
+#else
+  (void)clear;
+  return -1;
+#endif
 }
 
 }  // namespace mx

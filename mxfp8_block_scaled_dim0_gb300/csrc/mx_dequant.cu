@@ -46,6 +46,7 @@ struct DqParams {
   int64_t n_tiles;
   int32_t rpt;        // rows per tile band (256 / cpr when cpr < 256, else 1)
   int32_t cb4;        // ceil4(C / 32): padded scale columns
+  Span sp_out;        // for the bounds-checked build
 };
 
 // Four e4m3 bytes -> four f32 values (exact).
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kDqThreads) dequant_blocked_kernel(const DqPar
     }
 #pragma unroll
     for (int u = 0; u < kDqUnroll; ++u) {
-      if (ok[u])
+      if (ok[u] && in_span(p.sp_out, p.out + off[u], 16))
         *reinterpret_cast<uint4*>(p.out + off[u]) = dequant8(v[u], e8m0_value(sc[u]));
     }
   }
@@ -159,6 +160,7 @@ int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t
     p.n_tiles = (R + p.rpt - 1) / p.rpt;
   }
   p.cb4 = static_cast<int32_t>(((C / 32) + 3) / 4 * 4);
+  p.sp_out = make_span(out, 2 * static_cast<uint64_t>(R) * static_cast<uint64_t>(C));
   if (p.n_tiles > 0xFFFFFFFFll - 2ll * 65536 * 1024) return static_cast<int>(cudaErrorInvalidValue);
   // One wave of resident CTAs (as many per SM as registers allow) striding
   // over the tiles together.
@@ -186,5 +188,7 @@ int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t
   cfg.numAttrs = 1;
   return static_cast<int>(cudaLaunchKernelEx(&cfg, dequant_blocked_kernel, p));
 }
+
+int out_of_bounds_dequant(bool clear) { return read_out_of_bounds(clear); }
 
 }  // namespace mx

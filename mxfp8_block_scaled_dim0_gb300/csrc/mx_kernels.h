@@ -82,6 +82,14 @@ int launch_group_offsets(const int32_t* offs, int G, int64_t M, int64_t* row_off
 int launch_scales_to_blocked(const uint8_t* s, int64_t R, int64_t C, uint8_t* out,
                              cudaStream_t stream);
 int read_watchdog(int* out, bool clear);
+// Stores refused by the bounds-checked build, per translation unit (cleared
+// on request); -1 in a release build.
+int out_of_bounds_cast(bool clear);
+int out_of_bounds_blocked(bool clear);
+int out_of_bounds_dequant(bool clear);
+int out_of_bounds_scaled(bool clear);
+// -1 in a release build (nothing launched), else 0 or a cudaError_t value.
+int launch_bounds_selftest(void* buf, cudaStream_t stream);
 int read_scaled_watchdog(int* out, bool clear);   // the rowwise kernel's word (mx_scaled.cu)
 int launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t stream);
 

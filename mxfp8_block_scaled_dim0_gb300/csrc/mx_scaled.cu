@@ -88,7 +88,7 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
 }
 
 __global__ void __launch_bounds__(kThreads) tensor_amax_kernel(const uint16_t* x, int64_t n,
-                                                               uint32_t* amax_bits) {
+                                                               uint32_t* amax_bits, Span sp_amax) {
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ uint32_t red[kThreads / 32];
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) tensor_amax_kernel(const uint16_t* x
   if (blockIdx.x == 0 && threadIdx.x == 0)
     for (int64_t i = chunks << 3; i < n; ++i) m = max(m, static_cast<uint32_t>(x[i] & 0x7FFFu));
   m = block_max(m, red);
-  if (threadIdx.x == 0 && m != 0) atomicMax(amax_bits, m << 16);
+  if (threadIdx.x == 0 && m != 0 && in_span(sp_amax, amax_bits, 4)) atomicMax(amax_bits, m << 16);
 }
 
 __device__ __forceinline__ float tensor_scale(uint32_t amax_bits) {
@@ -124,15 +124,16 @@ __device__ __forceinline__ float tensor_scale(uint32_t amax_bits) {
 
 __global__ void __launch_bounds__(kThreads) tensorwise_kernel(const uint16_t* x, int64_t n,
                                                               const uint32_t* amax_bits,
-                                                              uint8_t* q, float* scale_out) {
+                                                              uint8_t* q, float* scale_out,
+                                                              Span sp_q, Span sp_scale) {
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const float s = tensor_scale(*amax_bits);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *scale_out = s;
+    if (in_span(sp_scale, scale_out, 4)) *scale_out = s;
     for (int64_t i = (n >> 3) << 3; i < n; ++i) {
       const float v = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
-      q[i] = static_cast<uint8_t>(e4m3x2(mul_rn(v, s), 0.0f) & 0xFFu);
+      if (in_span(sp_q, q + i, 1)) q[i] = static_cast<uint8_t>(e4m3x2(mul_rn(v, s), 0.0f) & 0xFFu);
     }
   }
   const int64_t chunks = n >> 3;
@@ -148,11 +149,11 @@ __global__ void __launch_bounds__(kThreads) tensorwise_kernel(const uint16_t* x,
     uint2 oa, ob;
     oa.x = e4m3x4(bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y), s);
     oa.y = e4m3x4(bf_lo(a.z), bf_hi(a.z), bf_lo(a.w), bf_hi(a.w), s);
-    reinterpret_cast<uint2*>(q)[c0] = oa;
+    if (in_span(sp_q, q + 8 * c0, 8)) reinterpret_cast<uint2*>(q)[c0] = oa;
     if (c1 >= 0) {
       ob.x = e4m3x4(bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y), s);
       ob.y = e4m3x4(bf_lo(b.z), bf_hi(b.z), bf_lo(b.w), bf_hi(b.w), s);
-      reinterpret_cast<uint2*>(q)[c1] = ob;
+      if (in_span(sp_q, q + 8 * c1, 8)) reinterpret_cast<uint2*>(q)[c1] = ob;
     }
   }
 }
@@ -188,13 +189,13 @@ __device__ __forceinline__ uint32_t row_e4m3x2(uint32_t w, float s, float r) {
 
 template <bool kFast>
 __device__ __forceinline__ void row_pass2(const uint4* xr, uint2* qr, int64_t chunks, int tid,
-                                          int T, float s, float r) {
+                                          int T, float s, float r, const Span& sq) {
   for (int64_t c = tid; c < chunks; c += T) {
     const uint4 a = __ldg(xr + c);
     uint2 o;
     o.x = row_e4m3x2<kFast>(a.x, s, r) | (row_e4m3x2<kFast>(a.y, s, r) << 16);
     o.y = row_e4m3x2<kFast>(a.z, s, r) | (row_e4m3x2<kFast>(a.w, s, r) << 16);
-    qr[c] = o;
+    if (in_span(sq, qr + c, 8)) qr[c] = o;
   }
 }
 
@@ -217,7 +218,8 @@ __device__ __forceinline__ uint16_t row_scale(uint32_t m, uint32_t* red, int g, 
 // group reads its row twice, the second time from L2.
 __global__ void __launch_bounds__(kThreads) rowwise_kernel(const uint16_t* x, int64_t M,
                                                            int64_t K, int t_log2, uint8_t* q,
-                                                           uint16_t* scale) {
+                                                           uint16_t* scale, Span sp_q,
+                                                           Span sp_scale) {
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ uint32_t red[kThreads / 32];
@@ -244,13 +246,13 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(const uint16_t* x, in
     const uint16_t sb = row_scale(mag_of(m), red, g, t_log2);
     if (!live) continue;
     const float s = __uint_as_float(static_cast<uint32_t>(sb) << 16);
-    if (tid == 0) scale[r] = sb;
+    if (tid == 0 && in_span(sp_scale, scale + r, 2)) scale[r] = sb;
     // Normal finite scales take the reciprocal path; zero, subnormal, Inf
     // and NaN scales the IEEE division.
     if (s >= FLT_MIN && s <= FLT_MAX)
-      row_pass2<true>(xr, qr, chunks, tid, T, s, div_rn(1.0f, s));
+      row_pass2<true>(xr, qr, chunks, tid, T, s, div_rn(1.0f, s), sp_q);
     else
-      row_pass2<false>(xr, qr, chunks, tid, T, s, 0.0f);
+      row_pass2<false>(xr, qr, chunks, tid, T, s, 0.0f, sp_q);
   }
 }
 
@@ -264,7 +266,8 @@ __device__ int g_scaled_watchdog = 0;
 
 __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* x, int64_t M,
                                                                 int64_t K, int t_log2, int stages,
-                                                                uint8_t* q, uint16_t* scale) {
+                                                                uint8_t* q, uint16_t* scale,
+                                                                Span sp_q, Span sp_scale) {
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(128) uint8_t ring[];
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
     const uint16_t sb = row_scale(mag_of(m), red, g, t_log2);
     const float sv = __uint_as_float(static_cast<uint32_t>(sb) << 16);
     if (live) {
-      if (tid == 0) scale[r] = sb;
+      if (tid == 0 && in_span(sp_scale, scale + r, 2)) scale[r] = sb;
       uint2* qr = reinterpret_cast<uint2*>(q + r * K);
       if (sv >= FLT_MIN && sv <= FLT_MAX) {
         const float rcp = div_rn(1.0f, sv);
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
           uint2 o;
           o.x = row_e4m3x2<true>(a.x, sv, rcp) | (row_e4m3x2<true>(a.y, sv, rcp) << 16);
           o.y = row_e4m3x2<true>(a.z, sv, rcp) | (row_e4m3x2<true>(a.w, sv, rcp) << 16);
-          qr[c] = o;
+          if (in_span(sp_q, qr + c, 8)) qr[c] = o;
         }
       } else {
         for (int64_t c = tid; c < chunks; c += T) {
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
           uint2 o;
           o.x = row_e4m3x2<false>(a.x, sv, 0.0f) | (row_e4m3x2<false>(a.y, sv, 0.0f) << 16);
           o.y = row_e4m3x2<false>(a.z, sv, 0.0f) | (row_e4m3x2<false>(a.w, sv, 0.0f) << 16);
-          qr[c] = o;
+          if (in_span(sp_q, qr + c, 8)) qr[c] = o;
         }
       }
     }
@@ -395,13 +398,16 @@ int launch_cast_tensorwise(const uint16_t* x, int64_t n, uint8_t* q, float* scal
   const int ga = static_cast<int>(chunks < want_a ? chunks : want_a);
   const int gc = static_cast<int>(chunks < want_c ? chunks : want_c);
   uint32_t* bits = reinterpret_cast<uint32_t*>(amax);
-  if (int rc = launch_pdl(tensor_amax_kernel, ga, stream, x, n, bits)) return rc;
+  if (int rc = launch_pdl(tensor_amax_kernel, ga, stream, x, n, bits, make_span(amax, 4)))
+    return rc;
   return launch_pdl(tensorwise_kernel, gc, stream, x, n, static_cast<const uint32_t*>(bits), q,
-                    scale);
+                    scale, make_span(q, static_cast<uint64_t>(n)), make_span(scale, 4));
 }
 
 int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint16_t* scale,
                         int num_sms, cudaStream_t stream) {
+  const Span sp_q = make_span(q, static_cast<uint64_t>(M) * static_cast<uint64_t>(K));
+  const Span sp_scale = make_span(scale, 2 * static_cast<uint64_t>(M));
   // Threads per row: enough for one 16-byte chunk each, 32 to 256.
   int t_log2 = 5;
   while (t_log2 < 8 && (int64_t{8} << (t_log2 + 1)) <= K) ++t_log2;
@@ -437,15 +443,17 @@ int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uin
     attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr_pdl;
     cfg.numAttrs = 1;
-    return static_cast<int>(
-        cudaLaunchKernelEx(&cfg, rowwise_bulk_kernel, x, M, K, t_log2, stages, q, scale));
+    return static_cast<int>(cudaLaunchKernelEx(&cfg, rowwise_bulk_kernel, x, M, K, t_log2, stages, q,
+                                               scale, sp_q, sp_scale));
   }
   static DeviceCache occ;
   const int per = occ.get([] { return wave(rowwise_kernel, 1); });
   const int64_t want = static_cast<int64_t>(num_sms) * per;
   const int grid = static_cast<int>(steps < want ? steps : want);
-  return launch_pdl(rowwise_kernel, grid, stream, x, M, K, t_log2, q, scale);
+  return launch_pdl(rowwise_kernel, grid, stream, x, M, K, t_log2, q, scale, sp_q, sp_scale);
 }
+
+int out_of_bounds_scaled(bool clear) { return read_out_of_bounds(clear); }
 
 int read_scaled_watchdog(int* out, bool clear) {
   int v = 0;

@@ -147,3 +147,18 @@ def test_scaled_fp8_entry_points_reject_bad_arguments(lib):
     assert lib.mx_cast_rowwise(A, 64, 12, A, A, None) == mx.MX_ERR_SHAPE
     assert lib.mx_cast_rowwise(A, 0, 64, A, A, None) == mx.MX_ERR_SHAPE
     assert lib.mx_cast_rowwise(A, 64, 64, B, A, None) == mx.MX_ERR_ALIGN
+
+
+def test_bounds_entry_points_in_release_build(lib):
+    """The release library has no checks compiled in: both report -1 without
+    touching a device."""
+    assert lib.mx_bounds_check(0) == -1
+    assert lib.mx_selftest_bounds(None, None) == mx.MX_ERR_NULL
+    assert lib.mx_selftest_bounds(A, None) == -1
+
+
+def test_bounds_checked_library_exports_every_symbol():
+    path = mxbuild.build(bounds=True)
+    blib = ctypes.CDLL(path)
+    for name in header_functions():
+        assert hasattr(blib, name), name
