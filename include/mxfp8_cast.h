@@ -3,9 +3,13 @@
  * block scales, blocks of 32) quantisation of bf16 matrices on sm_103a.
  *
  * Conventions for every entry point below
- *   - All data pointers are DEVICE pointers, allocated and owned by the
- *     caller; the library allocates no device memory and keeps no pointer
- *     after the call returns.
+ *   - All data pointers are DEVICE pointers of the calling thread's current
+ *     CUDA device (or managed memory), allocated and owned by the caller; the
+ *     library allocates no device memory and keeps no pointer after the call
+ *     returns.  Each pointer's memory type and device are checked on the
+ *     host (MX_ERR_DEVICE), so a host pointer or another device's pointer is
+ *     refused before any kernel sees it.  `stream` must belong to the same
+ *     device.
  *   - Every pointer must be 16-byte aligned (int32 / int64 offset arrays:
  *     4- / 8-byte aligned), tensors are dense row-major with no padding.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
@@ -58,7 +62,8 @@ enum {
   MX_ERR_SHAPE = -2,   /* a size is zero, negative, too large or not a multiple of 32 */
   MX_ERR_ALIGN = -3,   /* a pointer is not suitably aligned */
   MX_ERR_CUDA = -4,    /* a CUDA call failed (see mx_last_cuda_error) */
-  MX_ERR_GROUPS = -5   /* invalid group count, or (device status) invalid offsets */
+  MX_ERR_GROUPS = -5,  /* invalid group count, or (device status) invalid offsets */
+  MX_ERR_DEVICE = -6   /* a pointer is not device memory of the current device */
 };
 
 /* Fused dim0 + dim1 cast with both scale sets in blocked layout; one read of
@@ -240,8 +245,8 @@ int mx_bounds_check(int clear);
  * past an 8-byte span over `buf16` (16 bytes of device memory owned by the
  * caller, 16-byte aligned); the check refuses it, leaves bytes 8..11
  * untouched and adds one to the count read by mx_bounds_check().  Returns
- * MX_OK, MX_ERR_NULL / MX_ERR_ALIGN / MX_ERR_CUDA, or -1 in a release build
- * (nothing is launched). */
+ * MX_OK, MX_ERR_NULL / MX_ERR_ALIGN / MX_ERR_DEVICE / MX_ERR_CUDA, or -1 in
+ * a release build (nothing is launched). */
 int mx_selftest_bounds(void* buf16, void* stream);
 
 /* Diagnostic: enqueue one warp that waits, with a limit of `wait_ns`

@@ -2,7 +2,8 @@
 
 Thin ctypes layer over the C ABI of ``libmxfp8_cast.so`` (declared in
 ``include/mxfp8_cast.h``).  Functions named like the C entry points take torch
-tensors, check their shapes, and pass raw device pointers plus the current
+tensors, check their shapes and that they share one CUDA device, make that
+device current for the call, and pass raw device pointers plus its current
 CUDA stream; every step of the cast runs in the library's CUDA kernels.  There
 is no CPU fallback: if the library has not been built, importing the binding
 raises.
@@ -26,6 +27,7 @@ MX_ERR_SHAPE = -2
 MX_ERR_ALIGN = -3
 MX_ERR_CUDA = -4
 MX_ERR_GROUPS = -5
+MX_ERR_DEVICE = -6
 
 # Every function the header declares, for load checks.
 ABI_SYMBOLS = (
@@ -103,12 +105,45 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _stream(stream):
+# cudaStream_t (as an int) of a device's current stream; cheaper than
+# building a torch.cuda.Stream object per call.
+_raw_stream = torch._C._cuda_getCurrentRawStream
+
+
+def _stream(stream, dev=None):
+    """The call's cudaStream_t: `stream` (a torch.cuda.Stream or a raw
+    handle), else the current stream of device index `dev` (default: the
+    current device)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device() if dev is None else dev))
     if isinstance(stream, torch.cuda.Stream):
+        if dev is not None and stream.device_index != dev:
+            raise ValueError("stream is on cuda:%d, the tensors on cuda:%d"
+                             % (stream.device_index, dev))
         return ctypes.c_void_p(stream.cuda_stream)
     return ctypes.c_void_p(int(stream))
+
+
+def _device(*tensors):
+    """Index of the one CUDA device that all the call's tensors live on."""
+    devs = {t.get_device() for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError("all tensors of a call must be on one CUDA device, got %s"
+                         % ", ".join("cuda:%d" % d for d in sorted(devs)))
+    return devs.pop()
+
+
+def _call(name, dev, stream, *args):
+    """Call entry point `name` with device index `dev` current (the library
+    launches on the current device) and the stream appended: by default the
+    current stream of that device."""
+    fn = getattr(_lib(), name)
+    if torch.cuda.current_device() == dev:
+        rc = fn(*args, _stream(stream, dev))
+    else:
+        with torch.cuda.device(dev):
+            rc = fn(*args, _stream(stream, dev))
+    _check(rc, name)
 
 
 def _dev_tensor(t, name, nbytes=None, itemsize=None):
@@ -120,8 +155,8 @@ def _dev_tensor(t, name, nbytes=None, itemsize=None):
         raise ValueError("%s must be contiguous" % name)
     if itemsize is not None and t.element_size() != itemsize:
         raise TypeError("%s must have %d-byte elements" % (name, itemsize))
-    if nbytes is not None and t.numel() * t.element_size() < nbytes:
-        raise ValueError("%s holds %d bytes, needs %d" % (name, t.numel() * t.element_size(), nbytes))
+    if nbytes is not None and t.nbytes < nbytes:
+        raise ValueError("%s holds %d bytes, needs %d" % (name, t.nbytes, nbytes))
     return t
 
 
@@ -158,8 +193,9 @@ def mx_cast_dim0_dim1(x, q0, s0_blk, q1, s1_blk, stream=None):
     _dev_tensor(q1, "q1", M * K, 1)
     _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), 1)
     _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), 1)
-    _check(_lib().mx_cast_dim0_dim1(_ptr(x), M, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
-                                    _ptr(s1_blk), _stream(stream)), "mx_cast_dim0_dim1")
+    dev = _device(x, q0, s0_blk, q1, s1_blk)
+    _call("mx_cast_dim0_dim1", dev, stream, _ptr(x), M, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
+          _ptr(s1_blk))
 
 
 def mx_cast_dim0(x, q0, s0_blk, stream=None):
@@ -167,8 +203,7 @@ def mx_cast_dim0(x, q0, s0_blk, stream=None):
     M, K = x.shape
     _dev_tensor(q0, "q0", M * K, 1)
     _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), 1)
-    _check(_lib().mx_cast_dim0(_ptr(x), M, K, _ptr(q0), _ptr(s0_blk), _stream(stream)),
-           "mx_cast_dim0")
+    _call("mx_cast_dim0", _device(x, q0, s0_blk), stream, _ptr(x), M, K, _ptr(q0), _ptr(s0_blk))
 
 
 def mx_cast_dim1(x, q1, s1_blk, stream=None):
@@ -176,16 +211,14 @@ def mx_cast_dim1(x, q1, s1_blk, stream=None):
     M, K = x.shape
     _dev_tensor(q1, "q1", M * K, 1)
     _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), 1)
-    _check(_lib().mx_cast_dim1(_ptr(x), M, K, _ptr(q1), _ptr(s1_blk), _stream(stream)),
-           "mx_cast_dim1")
+    _call("mx_cast_dim1", _device(x, q1, s1_blk), stream, _ptr(x), M, K, _ptr(q1), _ptr(s1_blk))
 
 
 def mx_scales_to_blocked(s, out, stream=None):
     _dev_tensor(s, "s", itemsize=1)
     R, C = s.shape
     _dev_tensor(out, "out", mx_blocked_bytes(R, C), 1)
-    _check(_lib().mx_scales_to_blocked(_ptr(s), R, C, _ptr(out), _stream(stream)),
-           "mx_scales_to_blocked")
+    _call("mx_scales_to_blocked", _device(s, out), stream, _ptr(s), R, C, _ptr(out))
 
 
 def mx_cast_grouped_m(x, offs, q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs, status,
@@ -202,9 +235,9 @@ def mx_cast_grouped_m(x, offs, q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs,
     _dev_tensor(s0_row_offs, "s0_row_offs", 8 * (G + 1), 8)
     _dev_tensor(s1_col_offs, "s1_col_offs", 8 * (G + 1), 8)
     _dev_tensor(status, "status", 4, 4)
-    _check(_lib().mx_cast_grouped_m(_ptr(x), M, K, _ptr(offs), G, _ptr(q0), _ptr(s0_blk),
-                                    _ptr(s0_row_offs), _ptr(q1), _ptr(s1_blk), _ptr(s1_col_offs),
-                                    _ptr(status), _stream(stream)), "mx_cast_grouped_m")
+    dev = _device(x, offs, q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs, status)
+    _call("mx_cast_grouped_m", dev, stream, _ptr(x), M, K, _ptr(offs), G, _ptr(q0), _ptr(s0_blk),
+          _ptr(s0_row_offs), _ptr(q1), _ptr(s1_blk), _ptr(s1_col_offs), _ptr(status))
 
 
 def mx_cast_3d_dim1(w, q1, s1_blk, stream=None):
@@ -212,8 +245,8 @@ def mx_cast_3d_dim1(w, q1, s1_blk, stream=None):
     E, N, K = w.shape
     _dev_tensor(q1, "q1", E * N * K, 1)
     _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), 1)
-    _check(_lib().mx_cast_3d_dim1(_ptr(w), E, N, K, _ptr(q1), _ptr(s1_blk), _stream(stream)),
-           "mx_cast_3d_dim1")
+    dev = _device(w, q1, s1_blk)
+    _call("mx_cast_3d_dim1", dev, stream, _ptr(w), E, N, K, _ptr(q1), _ptr(s1_blk))
 
 
 def mx_cast_3d_dim0(w, q0, s0_blk, stream=None):
@@ -221,8 +254,8 @@ def mx_cast_3d_dim0(w, q0, s0_blk, stream=None):
     E, N, K = w.shape
     _dev_tensor(q0, "q0", E * N * K, 1)
     _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), 1)
-    _check(_lib().mx_cast_3d_dim0(_ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk), _stream(stream)),
-           "mx_cast_3d_dim0")
+    dev = _device(w, q0, s0_blk)
+    _call("mx_cast_3d_dim0", dev, stream, _ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk))
 
 
 def mx_cast_3d_dim0_dim1(w, q0, s0_blk, q1, s1_blk, stream=None):
@@ -232,8 +265,9 @@ def mx_cast_3d_dim0_dim1(w, q0, s0_blk, q1, s1_blk, stream=None):
     _dev_tensor(q1, "q1", E * N * K, 1)
     _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), 1)
     _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), 1)
-    _check(_lib().mx_cast_3d_dim0_dim1(_ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
-                                       _ptr(s1_blk), _stream(stream)), "mx_cast_3d_dim0_dim1")
+    dev = _device(w, q0, s0_blk, q1, s1_blk)
+    _call("mx_cast_3d_dim0_dim1", dev, stream, _ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
+          _ptr(s1_blk))
 
 
 def mx_dequant_blocked(q, s_blk, out, stream=None):
@@ -243,8 +277,8 @@ def mx_dequant_blocked(q, s_blk, out, stream=None):
     R, C = q.shape
     _dev_tensor(s_blk, "s_blk", mx_blocked_bytes(R, C // 32), 1)
     _dev_tensor(out, "out", 2 * R * C, 2)
-    _check(_lib().mx_dequant_blocked(_ptr(q), R, C, _ptr(s_blk), _ptr(out), _stream(stream)),
-           "mx_dequant_blocked")
+    dev = _device(q, s_blk, out)
+    _call("mx_dequant_blocked", dev, stream, _ptr(q), R, C, _ptr(s_blk), _ptr(out))
 
 
 def mx_cast_tensorwise(x, q, scale, amax, stream=None):
@@ -255,8 +289,8 @@ def mx_cast_tensorwise(x, q, scale, amax, stream=None):
     _dev_tensor(q, "q", n, 1)
     _dev_tensor(scale, "scale", 4, 4)
     _dev_tensor(amax, "amax", 4, 4)
-    _check(_lib().mx_cast_tensorwise(_ptr(x), n, _ptr(q), _ptr(scale), _ptr(amax),
-                                     _stream(stream)), "mx_cast_tensorwise")
+    dev = _device(x, q, scale, amax)
+    _call("mx_cast_tensorwise", dev, stream, _ptr(x), n, _ptr(q), _ptr(scale), _ptr(amax))
 
 
 def mx_cast_rowwise(x, q, scale, stream=None):
@@ -265,8 +299,7 @@ def mx_cast_rowwise(x, q, scale, stream=None):
     M, K = x.shape
     _dev_tensor(q, "q", M * K, 1)
     _dev_tensor(scale, "scale", 2 * M, 2)
-    _check(_lib().mx_cast_rowwise(_ptr(x), M, K, _ptr(q), _ptr(scale), _stream(stream)),
-           "mx_cast_rowwise")
+    _call("mx_cast_rowwise", _device(x, q, scale), stream, _ptr(x), M, K, _ptr(q), _ptr(scale))
 
 
 def mx_selftest_watchdog(wait_ns=50_000_000, stream=None):
@@ -288,7 +321,9 @@ def mx_selftest_bounds(buf16, stream=None):
     """Bounds-checked builds: one refused store just past an 8-byte span over
     buf16 (a 16-byte CUDA tensor); returns 0, or -1 in a release build."""
     _dev_tensor(buf16, "buf16", 16)
-    rc = _lib().mx_selftest_bounds(_ptr(buf16), _stream(stream))
+    dev = buf16.get_device()
+    with torch.cuda.device(dev):
+        rc = _lib().mx_selftest_bounds(_ptr(buf16), _stream(stream, dev))
     if rc < -1:
         raise MXError(rc, "mx_selftest_bounds")
     return rc

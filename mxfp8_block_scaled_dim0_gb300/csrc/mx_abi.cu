@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "mx_kernels.h"
@@ -130,6 +131,28 @@ int current_sm_count(int* sms) {
   return MX_OK;
 }
 
+// Every non-null pointer must be memory that the current device's kernels
+// may read and write: device memory of that device, or managed memory.  A
+// host pointer or another device's pointer would otherwise reach a kernel
+// (and its TMA descriptors) and fault there.
+int check_device(std::initializer_list<const void*> ptrs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(static_cast<int>(e));
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    cudaPointerAttributes a;
+    e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();   // leave no error behind for the caller's next check
+      return MX_ERR_DEVICE;
+    }
+    if (a.type == cudaMemoryTypeManaged) continue;
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return MX_ERR_DEVICE;
+  }
+  return MX_OK;
+}
+
 int check_2d_shape(int64_t M, int64_t K) {
   if (M < 32 || K < 32 || M > kMaxDim || K > kMaxDim) return MX_ERR_SHAPE;
   if (M % 32 != 0 || K % 32 != 0) return MX_ERR_SHAPE;
@@ -153,6 +176,7 @@ int cast_3d(const void* w, int64_t E, int64_t N, int64_t K, void* q0, void* s0_b
   if (!aligned(w, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16) || !aligned(q1, 16) ||
       !aligned(s1_blk, 16))
     return MX_ERR_ALIGN;
+  if (int rc = check_device({w, q0, s0_blk, q1, s1_blk})) return rc;
   const int64_t M = E * N;
   mx::CastMaps maps;
   if (int rc = encode_cast_maps(&maps, w, M, K, q1)) return rc;
@@ -209,6 +233,7 @@ const char* mx_strerror(int code) {
     case MX_ERR_ALIGN: return "misaligned pointer (16-byte alignment required)";
     case MX_ERR_CUDA: return "CUDA call failed (see mx_last_cuda_error)";
     case MX_ERR_GROUPS: return "invalid group count or group offsets";
+    case MX_ERR_DEVICE: return "pointer is not device memory of the current CUDA device";
     default: return "unknown error";
   }
 }
@@ -239,9 +264,13 @@ int mx_bounds_check(int clear) {
 int mx_selftest_bounds(void* buf16, void* stream) {
   if (!buf16) return MX_ERR_NULL;
   if (!aligned(buf16, 16)) return MX_ERR_ALIGN;
-  const int rc = mx::launch_bounds_selftest(buf16, static_cast<cudaStream_t>(stream));
-  if (rc == -1) return -1;
-  return launch_rc(rc);
+#ifndef MX_DEBUG_BOUNDS
+  (void)stream;
+  return -1;   // release build: no checks compiled in, nothing to launch
+#else
+  if (int rc = check_device({buf16})) return rc;
+  return launch_rc(mx::launch_bounds_selftest(buf16, static_cast<cudaStream_t>(stream)));
+#endif
 }
 
 int mx_selftest_watchdog(int64_t wait_ns, void* stream) {
@@ -257,6 +286,7 @@ int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_bl
   if (!aligned(x, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16) || !aligned(q1, 16) ||
       !aligned(s1_blk, 16))
     return MX_ERR_ALIGN;
+  if (int rc = check_device({x, q0, s0_blk, q1, s1_blk})) return rc;
   mx::CastMaps maps;
   if (int rc = encode_cast_maps(&maps, x, M, K, q1)) return rc;
   int sms = 0;
@@ -269,6 +299,7 @@ int mx_cast_dim1(const void* x, int64_t M, int64_t K, void* q1, void* s1_blk, vo
   if (!x || !q1 || !s1_blk) return MX_ERR_NULL;
   if (int rc = check_2d_shape(M, K)) return rc;
   if (!aligned(x, 16) || !aligned(q1, 16) || !aligned(s1_blk, 16)) return MX_ERR_ALIGN;
+  if (int rc = check_device({x, q1, s1_blk})) return rc;
   mx::CastMaps maps;
   if (int rc = encode_cast_maps(&maps, x, M, K, q1)) return rc;
   int sms = 0;
@@ -281,6 +312,7 @@ int mx_cast_dim0(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, vo
   if (!x || !q0 || !s0_blk) return MX_ERR_NULL;
   if (M < 1 || K < 32 || M > kMaxDim || K > kMaxDim || K % 32 != 0) return MX_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16)) return MX_ERR_ALIGN;
+  if (int rc = check_device({x, q0, s0_blk})) return rc;
   mx::CastMaps maps;
   if (int rc = encode_cast_maps(&maps, x, M, K, nullptr)) return rc;
   int sms = 0;
@@ -294,6 +326,7 @@ int mx_dequant_blocked(const void* q, int64_t R, int64_t C, const void* s_blk, v
   if (!q || !s_blk || !out) return MX_ERR_NULL;
   if (R < 1 || C < 32 || R > kMaxDim || C > kMaxDim || C % 32 != 0) return MX_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(s_blk, 16) || !aligned(out, 16)) return MX_ERR_ALIGN;
+  if (int rc = check_device({q, s_blk, out})) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   return launch_rc(mx::launch_dequant_blocked(static_cast<const uint8_t*>(q), R, C,
@@ -308,6 +341,7 @@ int mx_cast_tensorwise(const void* x, int64_t n, void* q, float* scale, float* a
   if (n < 1 || n > (int64_t{1} << 40)) return MX_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4) || !aligned(amax, 4))
     return MX_ERR_ALIGN;
+  if (int rc = check_device({x, q, scale, amax})) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   return launch_rc(mx::launch_cast_tensorwise(static_cast<const uint16_t*>(x), n,
@@ -319,6 +353,7 @@ int mx_cast_rowwise(const void* x, int64_t M, int64_t K, void* q, void* scale, v
   if (!x || !q || !scale) return MX_ERR_NULL;
   if (M < 1 || K < 8 || K % 8 != 0 || M > kMaxDim || K > kMaxDim) return MX_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 2)) return MX_ERR_ALIGN;
+  if (int rc = check_device({x, q, scale})) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
   return launch_rc(mx::launch_cast_rowwise(static_cast<const uint16_t*>(x), M, K,
@@ -330,6 +365,7 @@ int mx_scales_to_blocked(const void* s, int64_t R, int64_t C, void* out, void* s
   if (!s || !out) return MX_ERR_NULL;
   if (R < 1 || C < 1 || R > int64_t{65535} * 128 || C > kMaxDim) return MX_ERR_SHAPE;
   if (!aligned(out, 16)) return MX_ERR_ALIGN;
+  if (int rc = check_device({s, out})) return rc;
   return launch_rc(mx::launch_scales_to_blocked(static_cast<const uint8_t*>(s), R, C,
                                                 static_cast<uint8_t*>(out),
                                                 static_cast<cudaStream_t>(stream)));
@@ -347,6 +383,8 @@ int mx_cast_grouped_m(const void* x, int64_t M, int64_t K, const int32_t* offs, 
       !aligned(s1_blk, 16) || !aligned(offs, 4) || !aligned(s0_row_offs, 8) ||
       !aligned(s1_col_offs, 8) || !aligned(status, 4))
     return MX_ERR_ALIGN;
+  if (int rc = check_device({x, offs, q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs, status}))
+    return rc;
   mx::CastMaps maps;
   // q1 rows are 16-byte aligned only when M % 16 == 0; then whole tiles may
   // leave by TMA (see the grouped kernel), otherwise all of q1 is written with

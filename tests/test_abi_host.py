@@ -52,8 +52,32 @@ def test_size_helpers(lib):
 
 
 def test_strerror(lib):
-    for code in (0, -1, -2, -3, -4, -5, -99):
-        assert lib.mx_strerror(code)
+    texts = [lib.mx_strerror(code) for code in (0, -1, -2, -3, -4, -5, -6)]
+    assert all(texts) and len(set(texts)) == len(texts)
+    assert lib.mx_strerror(-99) == b"unknown error"
+
+
+def test_error_codes_match_header():
+    text = open(HEADER).read()
+    codes = dict((k, int(v)) for k, v in re.findall(r"\b(MX_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", text))
+    assert codes == {name: getattr(mx, name) for name in codes}
+    assert set(codes) == {n for n in dir(mx) if re.fullmatch(r"MX_(OK|ERR_\w+)", n)}
+
+
+class _OnDevice:
+    """Stands in for a CUDA tensor on device `index` (no GPU here)."""
+
+    def __init__(self, index):
+        self.index = index
+
+    def get_device(self):
+        return self.index
+
+
+def test_binding_refuses_tensors_on_several_devices():
+    assert mx._device(_OnDevice(1), None, _OnDevice(1)) == 1
+    with pytest.raises(ValueError, match="one CUDA device"):
+        mx._device(_OnDevice(0), _OnDevice(1))
 
 
 # Fake, never-dereferenced device addresses: argument checks run before any
