@@ -106,8 +106,10 @@ def _ptr(t):
 
 
 # cudaStream_t (as an int) of a device's current stream; cheaper than
-# building a torch.cuda.Stream object per call.
-_raw_stream = torch._C._cuda_getCurrentRawStream
+# building a torch.cuda.Stream object per call.  Builds of torch without the
+# raw accessor take the public route.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None) or (
+    lambda dev: torch.cuda.current_stream(dev).cuda_stream)
 
 
 def _stream(stream, dev=None):
