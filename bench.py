@@ -302,7 +302,8 @@ def make_row(row, args, dev, rank):
             def build(i):
                 return (gen(i), torch.empty((M, K), dtype=torch.uint8, device=dev),
                         torch.empty(M, dtype=torch.bfloat16, device=dev))
-            return Row("rowwise", wl, "rowwise_kernel", 2 * M * K + M * K + 2 * M, 1, build,
+            kernel = "rowwise_bulk_kernel" if K <= 24576 else "rowwise_kernel"
+            return Row("rowwise", wl, kernel, 2 * M * K + M * K + 2 * M, 1, build,
                        lambda a, st: mx.mx_cast_rowwise(*a, stream=st), (0,), (1, 2))
         if row == "dequant":
             # The dim0 copy of the workload (cast once, untimed) back to bf16.

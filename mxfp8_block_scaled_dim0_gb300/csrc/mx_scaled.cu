@@ -44,12 +44,14 @@ namespace mx {
 namespace {
 
 constexpr int kThreads = 256;
-// Bulk-staged rowwise: ring bytes per CTA.  Measured on GB300 at 16384^2 (one
-// 32 KB row per stage): 64 KB (2 stages, 3 CTAs per SM) 138.7 us; 96 KB
-// (2 CTAs per SM) 150.3 us; 128-160 KB (1 CTA per SM) 215.8 us; 512-thread
-// CTAs or a register cap for more resident CTAs were slower too.
-constexpr int64_t kRowRing = 64 * 1024;
-constexpr int64_t kMaxRowStage = 48 * 1024;   // largest stage (rows of one step) it takes
+// Bulk-staged rowwise: ring bytes per CTA (2 to 8 stages), and the largest
+// stage (rows of one step) it takes.  The launch shape (threads per row, ring
+// depth) follows a sweep on GB300 over K = 1024 ... 16384, every variant
+// byte-identical: e.g. 16640 x 5120 took 70.5 us with 256 threads per row and
+// 41.7 us with 64; 16384^2 took 135.2 us with two 32 KB stages per CTA and
+// 122.6 us with three.
+constexpr int64_t kRowRing = 48 * 1024;
+constexpr int64_t kMaxRowStage = 48 * 1024;
 
 __device__ __forceinline__ float div_rn(float a, float b) {
   float r;
@@ -408,16 +410,26 @@ int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uin
                         int num_sms, cudaStream_t stream) {
   const Span sp_q = make_span(q, static_cast<uint64_t>(M) * static_cast<uint64_t>(K));
   const Span sp_scale = make_span(scale, 2 * static_cast<uint64_t>(M));
-  // Threads per row: enough for one 16-byte chunk each, 32 to 256.
+  // Threads per row T = 2^t_log2: the power of two nearest to K / 64 (in the
+  // log domain), 32 to 256, so that each thread converts about eight 16-byte
+  // chunks of its row and the per-step barriers and reduction are amortised.
+  // t_log2 grows while K / 64 >= 2^(t_log2 + 1/2), i.e. K^2 >= 2^(2 t_log2 + 13).
   int t_log2 = 5;
-  while (t_log2 < 8 && (int64_t{8} << (t_log2 + 1)) <= K) ++t_log2;
+  const uint64_t k_sq = static_cast<uint64_t>(K) * static_cast<uint64_t>(K);
+  while (t_log2 < 8 && k_sq >= (uint64_t{1} << (2 * t_log2 + 13))) ++t_log2;
   const int64_t groups = kThreads >> t_log2;
   const int64_t steps = (M + groups - 1) / groups;
   const int64_t stage_bytes = groups * K * 2;
   if (stage_bytes <= kMaxRowStage) {
-    // Bulk-staged: as many stages (2..8) as fit in kRowRing bytes.
+    // Bulk-staged: as many stages (2..8) as fit in kRowRing bytes; three
+    // stages of 32 KB or more (96 KB, two CTAs per SM) where every CTA of such
+    // a grid runs at least 16 steps, so that the deeper ring pays for its
+    // fill.
     int stages = static_cast<int>(kRowRing / stage_bytes);
     stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+    if (stages == 2 && stage_bytes >= 32 * 1024 && 3 * stage_bytes <= 2 * kMaxRowStage &&
+        steps >= int64_t{32} * num_sms)
+      stages = 3;
     const int smem = static_cast<int>(stages * stage_bytes);
     static DeviceCache attr_cache;
     const int attr = attr_cache.get([] {

@@ -164,8 +164,12 @@ def test_tensorwise_full_size_sampled():
     assert_q_equal(to_np(q)[rows], oq, "sampled rows")
 
 
+# Launch shapes covered: 8, 4, 2 and 1 rows per bulk-staged step (32 to 256
+# threads per row), rings of 2, 3, 6 and 8 stages (39001 x 2048: three 32 KB
+# stages and a one-row last step), and the re-reading kernel for rows over
+# 24576 values.
 @pytest.mark.parametrize("M,K", [(1, 8), (3, 24), (77, 96), (256, 384), (64, 4128), (1000, 512),
-                                 (5, 16392), (3, 24584), (2, 40000)])
+                                 (37, 8200), (5, 16392), (3, 24584), (2, 40000), (39001, 2048)])
 def test_rowwise_matches_oracle(M, K):
     t = W.wide(M, K, 3 * M + K, zero_frac=0.02)
     compare_rowwise(W.bf16_bits(t), "%dx%d" % (M, K))
