@@ -8,11 +8,15 @@ written per element, plus the padded blocked scales) per second of device
 time, and its fraction of the measured GB300 copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mx|reference]
-                  [--row fused|dim1|grouped|experts|blocked] [--workload NAME]
+                  [--row ROW] [--workload NAME] [--shape ...] [--graph]
 
 --row times another row of the hot path instead (one JSON line each): the
-dim1-only cast, the grouped-M MoE cast (16640 x 5120, 4 groups), the 3D expert
-dim1 cast (16 x 8192 x 5120) or the standalone scale blocking (262144 x 512).
+dim0-only or dim1-only cast (dim0, dim1), the grouped-M MoE cast (grouped;
+16640 x 5120, 4 groups), the 3D expert casts (experts: dim1, experts0: dim0,
+experts01: both; 16 x 8192 x 5120), the standalone scale blocking (blocked;
+262144 x 512), MX dequantisation to bf16 (dequant) and the tensorwise and
+rowwise fp8 casts (tensorwise, rowwise; 16384 x 16384).  --graph replays the
+timed steps from CUDA graphs (for launch-bound small workloads).
 
 --impl reference times the CPU oracle (the plain C implementation used by the
 tests) on the host cores on a bounded sample of the same workload.  Under
