@@ -22,9 +22,12 @@
 // are short.  One wave of resident CTAs strides over the tiles together (all
 // CTAs work on neighbouring tiles at any time, which keeps DRAM accesses
 // local), two tiles' loads in flight per thread.  Measured on GB300 at
-// 16384^2: this read-1 / write-2 mix tops out near 5.9 TB/s even for a plain
-// zero-extending copy, which this kernel matches; four tiles per thread, 16
-// elements per thread, or contiguous per-CTA runs of tiles were 4-20% slower.
+// 16384^2: with 16-byte thread stores this read-1 / write-2 mix tops out near
+// 5.9 TB/s even for a plain zero-extending copy, which this kernel matches;
+// four tiles per thread, 16 elements per thread, or contiguous per-CTA runs
+// of tiles were 4-20% slower.  Staging 8192-element tiles in shared memory
+// and writing each with one bulk async copy was byte-identical but no faster
+// (slower for rows of 12288 values, faster only for rows of about 1024).
 #include <cuda_runtime.h>
 
 #include "mx_common.cuh"
