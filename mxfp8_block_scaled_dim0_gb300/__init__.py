@@ -14,6 +14,7 @@ Convenience wrappers (``cast_dim0_dim1``, ``cast_dim0``, ``cast_dim1``,
 ``cast_rowwise``) allocate outputs with torch and call the same entry points.
 """
 import ctypes
+import functools
 import os
 
 import torch
@@ -102,7 +103,8 @@ def library():
 # ---- marshalling helpers ----------------------------------------------------
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    # ctypes converts a plain int (or None) for a c_void_p parameter.
+    return t.data_ptr() if t is not None else None
 
 
 # cudaStream_t (as an int) of a device's current stream; cheaper than
@@ -117,13 +119,13 @@ def _stream(stream, dev=None):
     handle), else the current stream of device index `dev` (default: the
     current device)."""
     if stream is None:
-        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device() if dev is None else dev))
+        return _raw_stream(torch.cuda.current_device() if dev is None else dev)
     if isinstance(stream, torch.cuda.Stream):
         if dev is not None and stream.device_index != dev:
             raise ValueError("stream is on cuda:%d, the tensors on cuda:%d"
                              % (stream.device_index, dev))
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _device(*tensors):
@@ -169,18 +171,24 @@ def _check(rc, where):
 
 # ---- sizes ------------------------------------------------------------------
 
+# The size helpers are pure functions of their arguments; shapes repeat from
+# call to call, so their results are cached on the Python side.
+@functools.lru_cache(maxsize=4096)
 def mx_blocked_bytes(R, C):
     return int(_lib().mx_blocked_bytes(R, C))
 
 
+@functools.lru_cache(maxsize=4096)
 def mx_grouped_m_scale_bytes(M, K, G, dim):
     return int(_lib().mx_grouped_m_scale_bytes(M, K, G, dim))
 
 
+@functools.lru_cache(maxsize=4096)
 def mx_3d_scale_bytes(E, N, K):
     return int(_lib().mx_3d_scale_bytes(E, N, K))
 
 
+@functools.lru_cache(maxsize=4096)
 def mx_3d_dim0_scale_bytes(E, N, K):
     return int(_lib().mx_3d_dim0_scale_bytes(E, N, K))
 
