@@ -62,14 +62,17 @@ def _gen(seed: int, device) -> torch.Generator:
 def _pick_blocks(x: torch.Tensor, frac: float, g_cpu: torch.Generator):
     """Choose frac of the 32-blocks of a 2D tensor, half along rows and half
     along columns.  Returns (row_blocks, col_blocks) as (r, c0) index pairs:
-    row block = x[r, c0:c0+32], column block = x[r0:r0+32, c]."""
+    row block = x[r, c0:c0+32], column block = x[r0:r0+32, c].  Row blocks
+    are drawn from the M * (K // 32) whole blocks along rows; column blocks
+    from ceil(M / 32) * K, the last one cut short when M % 32 != 0.  (For M
+    and K multiples of 32 both counts are M * K / 32.)"""
     M, K = x.shape
     nb = (M * K) // 32
     n = int(round(frac * nb))
     n_row = n // 2
     n_col = n - n_row
-    rb = torch.randperm((M * K) // 32, generator=g_cpu)[:n_row]
-    cb = torch.randperm((M * K) // 32, generator=g_cpu)[:n_col]
+    rb = torch.randperm(M * (K // 32), generator=g_cpu)[:n_row]
+    cb = torch.randperm(((M + 31) // 32) * K, generator=g_cpu)[:n_col]
     row_blocks = [(int(i) // (K // 32), (int(i) % (K // 32)) * 32) for i in rb]
     col_blocks = [((int(i) // K) * 32, int(i) % K) for i in cb]
     return row_blocks, col_blocks

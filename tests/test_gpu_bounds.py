@@ -105,7 +105,10 @@ def test_3d_in_bounds(E, N, K):
     no_refused_stores()
 
 
-@pytest.mark.parametrize("M,K", [(1, 8), (77, 96), (1000, 512), (3, 24584)])
+# Rowwise launch shapes: 8 rows per step (8 and 6 stages), 2 rows per step,
+# three 32 KB stages with a one-row last step, and the re-reading kernel.
+@pytest.mark.parametrize("M,K", [(1, 8), (77, 96), (1000, 512), (37, 8200), (39001, 2048),
+                                 (3, 24584)])
 def test_scaled_fp8_in_bounds(M, K):
     x = W.wide(M, K, 7 * M + K, zero_frac=0.02)
     bits = W.bf16_bits(x)
