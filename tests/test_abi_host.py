@@ -186,3 +186,27 @@ def test_bounds_checked_library_exports_every_symbol():
     blib = ctypes.CDLL(path)
     for name in header_functions():
         assert hasattr(blib, name), name
+
+
+def test_c_program_compiles_links_and_calls_host_helpers(lib, tmp_path):
+    """The header is usable from plain C: a C99 program includes it, links
+    against the library and calls the host-only helpers (no GPU needed)."""
+    import subprocess
+    src = tmp_path / "use_abi.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "mxfp8_cast.h"\n'
+        "int main(void) {\n"
+        '  printf("%lld %lld %s\\n", (long long)mx_blocked_bytes(129, 5),\n'
+        "         (long long)mx_grouped_m_scale_bytes(16640, 5120, 4, 0),\n"
+        "         mx_strerror(MX_ERR_DEVICE));\n"
+        "  return mx_cast_dim0_dim1(0, 64, 64, 0, 0, 0, 0, 0) == MX_ERR_NULL ? 0 : 1;\n"
+        "}\n")
+    exe = tmp_path / "use_abi"
+    libdir = os.path.dirname(mx.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lmxfp8_cast",
+                    "-Wl,-rpath," + libdir], check=True, capture_output=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split()[:2] == [str(256 * 8), str((16640 + 512) * 160)]
+    assert "current" in r.stdout
