@@ -98,3 +98,27 @@ def test_kernel_hash_ignores_comments_and_layout():
     c = "int f(int x) { return x + 2; }\n"
     assert bench._code_tokens(a) == bench._code_tokens(b)
     assert bench._code_tokens(a) != bench._code_tokens(c)
+
+
+def test_reference_arm_prints_the_contract_line(capsys, monkeypatch):
+    """The reference arm (the oracle on the host cores) runs without a GPU:
+    one JSON line with every key the bench contract asks of it."""
+    import argparse
+    import json
+    for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    args = argparse.Namespace(gpus=1, steps=2, warmup=1)
+    assert bench.run_reference(args, budget_s=1.5) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["higher_is_better"] is True and line["vs_baseline"] is None
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "square16384_weight"
