@@ -181,24 +181,86 @@ def whole_job_value(bytes_per_step, steps, n_ranks, max_elapsed_s):
     return bytes_per_step * steps * n_ranks / max_elapsed_s / 1e9
 
 
+def roofline(bytes_per_step, launches, steps, elapsed_s, peak, peak_kind, kernel, traffic,
+             timing):
+    """Roofline record of one rank's timed region.  The steps run back to
+    back with no event between them, so a launch's duration is the region's
+    time over the launches in it; `achieved` is a step's algorithmic bytes
+    over a step's time (one launch per step for every row but the two-kernel
+    ones, where it covers both kernels of the step)."""
+    step_s = elapsed_s / steps
+    achieved = bytes_per_step / step_s / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+            "kernel": kernel, "launches_per_step": launches,
+            "avg_launch_us": 1e6 * step_s / launches,
+            "timing": timing + ", %d steps back to back, no events between them" % steps}
+
+
 # ---- CPU oracle timing (the CPU baseline and the reference arm) ---------------
 
-def time_oracle(seconds_budget=12.0, rows_per_slab=512):
+def host_cores():
+    """Host threads this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def time_oracle(seconds_budget=12.0, rows_per_slab=512, threads=1):
     """Time the oracle's fused cast (dim0 + dim1 + blocked scales) on row slabs
-    of the workload until the budget is spent.  Returns (GB/s, rows, seconds)."""
+    of the workload, on `threads` host threads, until the budget is spent.
+    Returns (GB/s, rows, seconds, threads used)."""
     import oracle
     from mxfp8_block_scaled_dim0_gb300 import workloads as W
     M, K = W.WORKLOADS[WORKLOAD].shape
     x = W.bf16_bits(W.normal((rows_per_slab, K), W.WORKLOADS[WORKLOAD].seed, std=0.02))
-    oracle.library_path()
-    done_rows, t_used = 0, 0.0
-    while done_rows == 0 or (t_used < seconds_budget and done_rows < M):
-        t0 = time.perf_counter()
-        oracle.cast_dim0_dim1_blocked(x)
-        t_used += time.perf_counter() - t0
-        done_rows += rows_per_slab
+    used = oracle.set_threads(threads)
+    try:
+        done_rows, t_used = 0, 0.0
+        while done_rows == 0 or (t_used < seconds_budget and done_rows < M):
+            t0 = time.perf_counter()
+            oracle.cast_dim0_dim1_blocked(x)
+            t_used += time.perf_counter() - t0
+            done_rows += rows_per_slab
+    finally:
+        oracle.set_threads(1)
     gbs = algorithmic_bytes(done_rows, K) / t_used / 1e9
-    return gbs, done_rows, t_used
+    return gbs, done_rows, t_used, used
+
+
+def cpu_baseline(seconds_budget):
+    """The oracle on all host cores and on one, on row slabs of the workload
+    (same value mix); the all-core figure is the baseline's value."""
+    n = host_cores()
+    gbs_n, rows_n, secs_n, used = time_oracle(seconds_budget * 2 / 3, rows_per_slab=2048, threads=n)
+    gbs_1, rows_1, secs_1, _ = time_oracle(seconds_budget / 3, rows_per_slab=512, threads=1)
+    return {"value": gbs_n, "unit": "GB/s", "cores": used, "kind": "oracle",
+            "sample": "first %d rows x 16384 cols of the 16384x16384 workload (same value mix), "
+                      "%.1f s, fused dim0+dim1+blocked scales, %d threads (OpenMP over rows / "
+                      "columns)" % (rows_n, secs_n, used),
+            "cores_1": {"value": gbs_1, "unit": "GB/s",
+                        "sample": "first %d rows, %.1f s, single thread" % (rows_1, secs_1)},
+            "nproc": n, "cpu_model": cpu_model()}
 
 
 def run_reference(args, budget_s=90.0):
@@ -212,21 +274,27 @@ def run_reference(args, budget_s=90.0):
     from mxfp8_block_scaled_dim0_gb300 import workloads as W
     M, K = W.WORKLOADS[WORKLOAD].shape
     seed = W.WORKLOADS[WORKLOAD].seed
-    calib = W.bf16_bits(W.normal((32, K), seed, std=0.02))
-    oracle.library_path()
-    t0 = time.perf_counter()
-    oracle.cast_dim0_dim1_blocked(calib)
-    t_row = (time.perf_counter() - t0) / 32
-    rows = int(budget_s / (args.steps + args.warmup) / t_row) // 32 * 32
-    rows = max(32, min(M, rows))
-    x = W.bf16_bits(W.normal((rows, K), seed, std=0.02))
-    times = []
-    for i in range(args.warmup + args.steps):
+    n = host_cores()
+    # Single-thread figure on a small slab, for the record.
+    gbs_1, rows_1, secs_1, _ = time_oracle(min(3.0, budget_s / 10), rows_per_slab=256, threads=1)
+    used = oracle.set_threads(n)
+    try:
+        calib = W.bf16_bits(W.normal((32 * n, K), seed, std=0.02))
         t0 = time.perf_counter()
-        oracle.cast_dim0_dim1_blocked(x)
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            times.append(dt)
+        oracle.cast_dim0_dim1_blocked(calib)
+        t_row = (time.perf_counter() - t0) / (32 * n)
+        rows = int(budget_s * 0.9 / (args.steps + args.warmup) / t_row) // 32 * 32
+        rows = max(32, min(M, rows))
+        x = W.bf16_bits(W.normal((rows, K), seed, std=0.02))
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.cast_dim0_dim1_blocked(x)
+            dt = time.perf_counter() - t0
+            if i >= args.warmup:
+                times.append(dt)
+    finally:
+        oracle.set_threads(1)
     t = sum(times)
     rows_total = rows * len(times)
     value = algorithmic_bytes(rows, K) * len(times) / t / 1e9
@@ -237,8 +305,12 @@ def run_reference(args, budget_s=90.0):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "shape": [16384, 16384],
                    "sample": "%d-row slab of the workload per step (bounded CPU sample)" % rows},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d rows x %d cols over %d steps" % (rows_total, K, len(times))},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": "%d rows x %d cols over %d steps, %d threads"
+                                   % (rows_total, K, len(times), used),
+                         "cores_1": {"value": gbs_1, "unit": "GB/s",
+                                     "sample": "%d rows, %.1f s, single thread" % (rows_1, secs_1)},
+                         "nproc": n, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -403,6 +475,14 @@ def run_gpu(args):
     import mxfp8_block_scaled_dim0_gb300 as mx
     mx.library()
 
+    # Clock samples cover the timed region; nvidia-smi starts now, while the
+    # buffers are built, so that no idle pause is needed before timing (a
+    # GPU left idle before the timed region ran its first steps slower).
+    gpu_index = dev.index if ws > 1 else int(
+        (os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0").strip() or 0)
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+
     R = make_row(args.row, args, dev, rank)
     nbytes = R.bytes_per_step
     stream = torch.cuda.current_stream(dev)
@@ -430,45 +510,29 @@ def run_gpu(args):
         graph.replay()
         torch.cuda.synchronize(dev)
 
-    # Timed region: K steps between two events; every 8th step also gets its
-    # own event pair, for the per-launch duration of the kernel (graph mode:
-    # the per-step time of the replayed graph).
-    every = 8
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(0, args.steps, every)] if graph is None else []
+    # Timed region: K steps back to back between two events on the launching
+    # stream.  No event is recorded between steps: an event between two
+    # programmatic-dependent launches would end their overlap and add launch
+    # latency to what it measures.
     t_beg = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    gpu_index = dev.index if ws > 1 else int(
-        (os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0").strip() or 0)
-    clocks = ClockSampler(gpu_index)
     barrier(ws)
     torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.15)
     t_beg.record(stream)
     if graph is not None:
         for _ in range(args.steps // per_graph):
             graph.replay()
     else:
         for i in range(args.steps):
-            if i % every == 0:
-                ev[i // every][0].record(stream)
-                step(i)
-                ev[i // every][1].record(stream)
-            else:
-                step(i)
+            step(i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clock_info = clocks.stop()
     barrier(ws)
     elapsed = t_beg.elapsed_time(t_end) / 1e3
-    per_launch = ([a.elapsed_time(b) / 1e3 for a, b in ev] if graph is None
-                  else [elapsed / args.steps])
     max_elapsed = max_over_ranks(elapsed, ws, dev)
     value = whole_job_value(nbytes, args.steps, ws, max_elapsed)
-    avg_launch = sum(per_launch) / len(per_launch)
     peak, peak_kind = hbm_peak()
-    achieved = nbytes / avg_launch / 1e9
 
     # End to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory, calls the cast, and copies every
@@ -516,11 +580,7 @@ def run_gpu(args):
     cpu = None
     if (rank == 0 and ws == 1 and args.cpu_seconds > 0 and R.name == "fused" and not args.shape
             and not args.workload):
-        gbs, rows, secs = time_oracle(seconds_budget=args.cpu_seconds)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "first %d rows x 16384 cols of the 16384x16384 workload (same value "
-                         "mix), %.1f s, fused dim0+dim1+blocked scales, single thread"
-                         % (rows, secs)}
+        cpu = cpu_baseline(args.cpu_seconds)
 
     if rank == 0:
         shape = list(sets[0][0].shape)
@@ -536,13 +596,10 @@ def run_gpu(args):
                        "l2": "inputs %d MiB each, two buffer sets alternated (L2 is 129 MB)"
                              % (sets[0][0].numel() * sets[0][0].element_size() >> 20),
                        "parallelism": "replicas" if ws > 1 else "single"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": measured_traffic() if R.name == "fused" and not args.shape
-                         and not args.workload else None,
-                         "kernel": R.kernel, "avg_launch_us": 1e6 * avg_launch,
-                         "launch_samples": len(per_launch),
-                         "timing": "cuda graph replay" if graph is not None else "stream launches"},
+            "roofline": roofline(nbytes, R.launches, args.steps, elapsed, peak, peak_kind,
+                                 R.kernel, measured_traffic() if R.name == "fused"
+                                 and not args.shape and not args.workload else None,
+                                 "cuda graph replay" if graph is not None else "stream launches"),
             "frac_of_peak": value / ws / peak,
             # the pages' nominal HBM figure (8 TB/s), beside the measured copy peak
             "frac_of_nominal": {"value": value / ws / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS},

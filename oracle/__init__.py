@@ -66,6 +66,10 @@ def _configure(lib):
     lib.oracle_cast_tensorwise.restype = None
     lib.oracle_cast_rowwise.argtypes = [P, I64, I64, P, P]
     lib.oracle_cast_rowwise.restype = None
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_threads.restype = None
+    lib.oracle_threads.argtypes = []
+    lib.oracle_threads.restype = ctypes.c_int
     return lib
 
 
@@ -89,6 +93,21 @@ def _bits(x):
 
 def _cdiv(a, b):
     return -(-a // b)
+
+
+# ---- host threads ---------------------------------------------------------------
+
+def set_threads(n: int) -> int:
+    """Spread the dim0 / dim1 casts (and every call built on them) over n
+    host threads; returns the count in effect (1 if the library was built
+    without OpenMP).  The result does not depend on it."""
+    lib = _load()
+    lib.oracle_set_threads(int(n))
+    return int(lib.oracle_threads())
+
+
+def threads() -> int:
+    return int(_load().oracle_threads())
 
 
 # ---- scalar encodings -------------------------------------------------------

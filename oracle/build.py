@@ -22,10 +22,13 @@ def build(force: bool = False) -> str:
         return LIB
     tmp = LIB + ".tmp.%d" % os.getpid()
     # -O2 without -ffast-math: the oracle relies on IEEE double semantics and
-    # on nearbyint() rounding ties to even.
+    # on nearbyint() rounding ties to even.  OpenMP only spreads independent
+    # rows / columns over host threads (oracle_set_threads); where the
+    # compiler has no OpenMP runtime the oracle is built sequential.
     cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-fPIC", "-shared",
            "-Wall", "-Wextra", "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    if subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True).returncode != 0:
+        subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -45,6 +45,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define MX_BLOCK 32
 #define E4M3_EMAX 8          /* largest normal e4m3 is 1.75 * 2^8 */
@@ -147,15 +150,39 @@ static void cast_block(const double *blk, int n, uint8_t s, uint8_t *q)
     }
 }
 
+/* ---- threads ---------------------------------------------------------- */
+
+/* Host threads that the dim0 and dim1 casts spread their rows / columns over.
+ * Every row (dim0) or column (dim1) is computed by the same scalar code on its
+ * own, so the result does not depend on the count; 1 (the default) runs the
+ * plain sequential loops.  Built without OpenMP, the count is ignored. */
+static int g_threads = 1;
+
+void oracle_set_threads(int n)
+{
+    g_threads = n < 1 ? 1 : n;
+}
+
+/* Threads the casts will use (1 when built without OpenMP). */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return g_threads;
+#else
+    return 1;
+#endif
+}
+
 /* ---- directions ------------------------------------------------------- */
 
 /* dim0: blocks of 32 along each row of x (M x K, row-major bf16 bits).
  * q: M x K bytes, s: M x (K/32) bytes (plain, unswizzled).  K % 32 == 0. */
 void oracle_cast_dim0(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, uint8_t *s)
 {
-    double blk[MX_BLOCK];
     int64_t Kb = K / MX_BLOCK;
+#pragma omp parallel for num_threads(g_threads) schedule(static)
     for (int64_t r = 0; r < M; r++) {
+        double blk[MX_BLOCK];
         for (int64_t j = 0; j < Kb; j++) {
             for (int i = 0; i < MX_BLOCK; i++)
                 blk[i] = oracle_bf16_to_double(x[r * K + j * MX_BLOCK + i]);
@@ -172,10 +199,11 @@ void oracle_cast_dim0(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, uint8
  * that dim1(X) == dim0(X^T) is a check rather than a tautology. */
 void oracle_cast_dim1(const uint16_t *x, int64_t M, int64_t K, uint8_t *q, uint8_t *s)
 {
-    double blk[MX_BLOCK];
-    uint8_t qb[MX_BLOCK];
     int64_t Mb = M / MX_BLOCK;
+#pragma omp parallel for num_threads(g_threads) schedule(static)
     for (int64_t k = 0; k < K; k++) {
+        double blk[MX_BLOCK];
+        uint8_t qb[MX_BLOCK];
         for (int64_t j = 0; j < Mb; j++) {
             for (int i = 0; i < MX_BLOCK; i++)
                 blk[i] = oracle_bf16_to_double(x[(j * MX_BLOCK + i) * K + k]);

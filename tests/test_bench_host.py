@@ -21,6 +21,35 @@ def test_whole_job_value():
     assert bench.whole_job_value(1e9, 10, 2, 4.0) == pytest.approx(5.0)
 
 
+def test_roofline_launch_time_is_bounded_by_the_step_time():
+    # One launch per step: the launch's time is the step's time, and the
+    # fraction follows from the bytes over it.
+    nbytes, steps, elapsed = 1_090_519_040, 20, 20 * 171.9e-6
+    r = bench.roofline(nbytes, 1, steps, elapsed, 6791.4, "measured", "k", None, "stream launches")
+    ms_per_step = 1e3 * elapsed / steps
+    assert r["avg_launch_us"] <= 1000 * ms_per_step / r["launches_per_step"] + 1e-9
+    assert r["achieved"] == pytest.approx(nbytes / (elapsed / steps) / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6791.4)
+    assert r["frac"] == pytest.approx(bench.whole_job_value(nbytes, steps, 1, elapsed) / 6791.4)
+    # Two launches per step (tensorwise): each averages half of the step.
+    r2 = bench.roofline(nbytes, 2, steps, elapsed, 6791.4, "measured", "k", None, "x")
+    assert r2["avg_launch_us"] == pytest.approx(1000 * ms_per_step / 2)
+    assert r2["achieved"] == pytest.approx(r["achieved"])
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in r
+
+
+def test_cpu_baseline_record():
+    cb = bench.cpu_baseline(0.3)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    assert cb["nproc"] == bench.host_cores() >= 1
+    assert 1 <= cb["cores"] <= cb["nproc"]
+    assert cb["cores_1"]["value"] > 0 and cb["cores_1"]["unit"] == "GB/s"
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+    import oracle
+    assert oracle.threads() == 1   # timing leaves the oracle sequential
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
@@ -119,6 +148,7 @@ def test_reference_arm_prints_the_contract_line(capsys, monkeypatch):
     assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert cb["nproc"] >= cb["cores"] and cb["cores_1"]["value"] > 0 and cb["cpu_model"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == "square16384_weight"
