@@ -38,7 +38,7 @@ ABI_SYMBOLS = (
     "mx_3d_dim0_scale_bytes", "mx_cast_tensorwise", "mx_cast_rowwise", "mx_bounds_check",
     "mx_selftest_bounds",
     "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
-    "mx_selftest_watchdog",
+    "mx_selftest_watchdog", "mx_selftest_arm_stall",
 )
 
 
@@ -86,6 +86,7 @@ def _lib():
             "mx_bounds_check": ([ctypes.c_int], ctypes.c_int),
             "mx_selftest_bounds": ([P, P], ctypes.c_int),
             "mx_selftest_watchdog": ([I64, P], ctypes.c_int),
+            "mx_selftest_arm_stall": ([I64, I64], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -131,6 +132,9 @@ def _stream(stream, dev=None):
 def _device(*tensors):
     """Index of the one CUDA device that all the call's tensors live on."""
     devs = {t.get_device() for t in tensors if t is not None}
+    if any(d < 0 for d in devs):
+        raise ValueError("every tensor of a call must be a CUDA tensor, got %s"
+                         % ", ".join(sorted({str(t.device) for t in tensors if t is not None})))
     if len(devs) != 1:
         raise ValueError("all tensors of a call must be on one CUDA device, got %s"
                          % ", ".join("cuda:%d" % d for d in sorted(devs)))
@@ -150,15 +154,27 @@ def _call(name, dev, stream, *args):
     _check(rc, name)
 
 
-def _dev_tensor(t, name, nbytes=None, itemsize=None):
+# dtypes each kind of argument may have.  The C ABI sees only pointers, so
+# this is the one place where a float16 tensor passed as bf16 input, or float
+# offsets passed as int32 group ends, can be refused.
+BF16 = (torch.bfloat16,)
+BYTES = tuple(d for d in (torch.uint8, getattr(torch, "float8_e4m3fn", None),
+                          getattr(torch, "float8_e8m0fnu", None)) if d is not None)
+I32 = (torch.int32,)
+I64 = (torch.int64,)
+F32 = (torch.float32,)
+
+
+def _dev_tensor(t, name, nbytes=None, dtypes=None, ndim=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
-    if not t.is_cuda:
-        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError("%s must have dtype %s, got %s"
+                        % (name, " or ".join(str(d) for d in dtypes), t.dtype))
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dimensions, got shape %s" % (name, ndim, tuple(t.shape)))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
-    if itemsize is not None and t.element_size() != itemsize:
-        raise TypeError("%s must have %d-byte elements" % (name, itemsize))
     if nbytes is not None and t.nbytes < nbytes:
         raise ValueError("%s holds %d bytes, needs %d" % (name, t.nbytes, nbytes))
     return t
@@ -197,84 +213,84 @@ def mx_3d_dim0_scale_bytes(E, N, K):
 
 def mx_cast_dim0_dim1(x, q0, s0_blk, q1, s1_blk, stream=None):
     """Fused dim0 + dim1 cast of bf16 x (M x K) into caller buffers."""
-    _dev_tensor(x, "x", itemsize=2)
+    _dev_tensor(x, "x", dtypes=BF16, ndim=2)
     M, K = x.shape
-    _dev_tensor(q0, "q0", M * K, 1)
-    _dev_tensor(q1, "q1", M * K, 1)
-    _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), 1)
-    _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), 1)
+    _dev_tensor(q0, "q0", M * K, BYTES)
+    _dev_tensor(q1, "q1", M * K, BYTES)
+    _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), BYTES)
+    _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), BYTES)
     dev = _device(x, q0, s0_blk, q1, s1_blk)
     _call("mx_cast_dim0_dim1", dev, stream, _ptr(x), M, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
           _ptr(s1_blk))
 
 
 def mx_cast_dim0(x, q0, s0_blk, stream=None):
-    _dev_tensor(x, "x", itemsize=2)
+    _dev_tensor(x, "x", dtypes=BF16, ndim=2)
     M, K = x.shape
-    _dev_tensor(q0, "q0", M * K, 1)
-    _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), 1)
+    _dev_tensor(q0, "q0", M * K, BYTES)
+    _dev_tensor(s0_blk, "s0_blk", mx_blocked_bytes(M, K // 32), BYTES)
     _call("mx_cast_dim0", _device(x, q0, s0_blk), stream, _ptr(x), M, K, _ptr(q0), _ptr(s0_blk))
 
 
 def mx_cast_dim1(x, q1, s1_blk, stream=None):
-    _dev_tensor(x, "x", itemsize=2)
+    _dev_tensor(x, "x", dtypes=BF16, ndim=2)
     M, K = x.shape
-    _dev_tensor(q1, "q1", M * K, 1)
-    _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), 1)
+    _dev_tensor(q1, "q1", M * K, BYTES)
+    _dev_tensor(s1_blk, "s1_blk", mx_blocked_bytes(K, M // 32), BYTES)
     _call("mx_cast_dim1", _device(x, q1, s1_blk), stream, _ptr(x), M, K, _ptr(q1), _ptr(s1_blk))
 
 
 def mx_scales_to_blocked(s, out, stream=None):
-    _dev_tensor(s, "s", itemsize=1)
+    _dev_tensor(s, "s", dtypes=BYTES, ndim=2)
     R, C = s.shape
-    _dev_tensor(out, "out", mx_blocked_bytes(R, C), 1)
+    _dev_tensor(out, "out", mx_blocked_bytes(R, C), BYTES)
     _call("mx_scales_to_blocked", _device(s, out), stream, _ptr(s), R, C, _ptr(out))
 
 
 def mx_cast_grouped_m(x, offs, q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs, status,
                       stream=None):
-    _dev_tensor(x, "x", itemsize=2)
+    _dev_tensor(x, "x", dtypes=BF16, ndim=2)
     M, K = x.shape
-    _dev_tensor(offs, "offs", itemsize=4)
+    _dev_tensor(offs, "offs", dtypes=I32, ndim=1)
     G = offs.numel()
-    _dev_tensor(q0, "q0", M * K, 1)
-    _dev_tensor(q1, "q1", M * K, 1)
+    _dev_tensor(q0, "q0", M * K, BYTES)
+    _dev_tensor(q1, "q1", M * K, BYTES)
     if G >= 1:
-        _dev_tensor(s0_blk, "s0_blk", mx_grouped_m_scale_bytes(M, K, G, 0), 1)
-        _dev_tensor(s1_blk, "s1_blk", mx_grouped_m_scale_bytes(M, K, G, 1), 1)
-    _dev_tensor(s0_row_offs, "s0_row_offs", 8 * (G + 1), 8)
-    _dev_tensor(s1_col_offs, "s1_col_offs", 8 * (G + 1), 8)
-    _dev_tensor(status, "status", 4, 4)
+        _dev_tensor(s0_blk, "s0_blk", mx_grouped_m_scale_bytes(M, K, G, 0), BYTES)
+        _dev_tensor(s1_blk, "s1_blk", mx_grouped_m_scale_bytes(M, K, G, 1), BYTES)
+    _dev_tensor(s0_row_offs, "s0_row_offs", 8 * (G + 1), I64)
+    _dev_tensor(s1_col_offs, "s1_col_offs", 8 * (G + 1), I64)
+    _dev_tensor(status, "status", 4, I32)
     dev = _device(x, offs, q0, s0_blk, s0_row_offs, q1, s1_blk, s1_col_offs, status)
     _call("mx_cast_grouped_m", dev, stream, _ptr(x), M, K, _ptr(offs), G, _ptr(q0), _ptr(s0_blk),
           _ptr(s0_row_offs), _ptr(q1), _ptr(s1_blk), _ptr(s1_col_offs), _ptr(status))
 
 
 def mx_cast_3d_dim1(w, q1, s1_blk, stream=None):
-    _dev_tensor(w, "w", itemsize=2)
+    _dev_tensor(w, "w", dtypes=BF16, ndim=3)
     E, N, K = w.shape
-    _dev_tensor(q1, "q1", E * N * K, 1)
-    _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), 1)
+    _dev_tensor(q1, "q1", E * N * K, BYTES)
+    _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), BYTES)
     dev = _device(w, q1, s1_blk)
     _call("mx_cast_3d_dim1", dev, stream, _ptr(w), E, N, K, _ptr(q1), _ptr(s1_blk))
 
 
 def mx_cast_3d_dim0(w, q0, s0_blk, stream=None):
-    _dev_tensor(w, "w", itemsize=2)
+    _dev_tensor(w, "w", dtypes=BF16, ndim=3)
     E, N, K = w.shape
-    _dev_tensor(q0, "q0", E * N * K, 1)
-    _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), 1)
+    _dev_tensor(q0, "q0", E * N * K, BYTES)
+    _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), BYTES)
     dev = _device(w, q0, s0_blk)
     _call("mx_cast_3d_dim0", dev, stream, _ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk))
 
 
 def mx_cast_3d_dim0_dim1(w, q0, s0_blk, q1, s1_blk, stream=None):
-    _dev_tensor(w, "w", itemsize=2)
+    _dev_tensor(w, "w", dtypes=BF16, ndim=3)
     E, N, K = w.shape
-    _dev_tensor(q0, "q0", E * N * K, 1)
-    _dev_tensor(q1, "q1", E * N * K, 1)
-    _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), 1)
-    _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), 1)
+    _dev_tensor(q0, "q0", E * N * K, BYTES)
+    _dev_tensor(q1, "q1", E * N * K, BYTES)
+    _dev_tensor(s0_blk, "s0_blk", mx_3d_dim0_scale_bytes(E, N, K), BYTES)
+    _dev_tensor(s1_blk, "s1_blk", mx_3d_scale_bytes(E, N, K), BYTES)
     dev = _device(w, q0, s0_blk, q1, s1_blk)
     _call("mx_cast_3d_dim0_dim1", dev, stream, _ptr(w), E, N, K, _ptr(q0), _ptr(s0_blk), _ptr(q1),
           _ptr(s1_blk))
@@ -283,10 +299,10 @@ def mx_cast_3d_dim0_dim1(w, q0, s0_blk, q1, s1_blk, stream=None):
 def mx_dequant_blocked(q, s_blk, out, stream=None):
     """bf16 out (R x C) = e4m3 q (R x C) times 2^(scale - 127), scales in
     blocked layout."""
-    _dev_tensor(q, "q", itemsize=1)
+    _dev_tensor(q, "q", dtypes=BYTES, ndim=2)
     R, C = q.shape
-    _dev_tensor(s_blk, "s_blk", mx_blocked_bytes(R, C // 32), 1)
-    _dev_tensor(out, "out", 2 * R * C, 2)
+    _dev_tensor(s_blk, "s_blk", mx_blocked_bytes(R, C // 32), BYTES)
+    _dev_tensor(out, "out", 2 * R * C, BF16)
     dev = _device(q, s_blk, out)
     _call("mx_dequant_blocked", dev, stream, _ptr(q), R, C, _ptr(s_blk), _ptr(out))
 
@@ -294,21 +310,21 @@ def mx_dequant_blocked(q, s_blk, out, stream=None):
 def mx_cast_tensorwise(x, q, scale, amax, stream=None):
     """Tensorwise fp8 of bf16 x (any shape): q (x.numel() bytes), scale and
     amax (one float32 each)."""
-    _dev_tensor(x, "x", itemsize=2)
+    _dev_tensor(x, "x", dtypes=BF16)
     n = x.numel()
-    _dev_tensor(q, "q", n, 1)
-    _dev_tensor(scale, "scale", 4, 4)
-    _dev_tensor(amax, "amax", 4, 4)
+    _dev_tensor(q, "q", n, BYTES)
+    _dev_tensor(scale, "scale", 4, F32)
+    _dev_tensor(amax, "amax", 4, F32)
     dev = _device(x, q, scale, amax)
     _call("mx_cast_tensorwise", dev, stream, _ptr(x), n, _ptr(q), _ptr(scale), _ptr(amax))
 
 
 def mx_cast_rowwise(x, q, scale, stream=None):
     """Rowwise fp8 of bf16 x (M x K): q (M x K bytes), scale (M bf16)."""
-    _dev_tensor(x, "x", itemsize=2)
+    _dev_tensor(x, "x", dtypes=BF16, ndim=2)
     M, K = x.shape
-    _dev_tensor(q, "q", M * K, 1)
-    _dev_tensor(scale, "scale", 2 * M, 2)
+    _dev_tensor(q, "q", M * K, BYTES)
+    _dev_tensor(scale, "scale", 2 * M, BF16)
     _call("mx_cast_rowwise", _device(x, q, scale), stream, _ptr(x), M, K, _ptr(q), _ptr(scale))
 
 
@@ -316,6 +332,13 @@ def mx_selftest_watchdog(wait_ns=50_000_000, stream=None):
     """Run the bounded-wait failure path on the device (no fault): a warp
     waits on a barrier that never completes and gives up after wait_ns."""
     _check(_lib().mx_selftest_watchdog(int(wait_ns), _stream(stream)), "mx_selftest_watchdog")
+
+
+def mx_selftest_arm_stall(at, wait_ns=20_000_000):
+    """Arm a stall for this thread's next cast (or bulk-staged rowwise)
+    launch: CTA 0 gives up waiting at its `at`-th tile and takes the abort
+    path, without any fault (see include/mxfp8_cast.h)."""
+    _check(_lib().mx_selftest_arm_stall(int(at), int(wait_ns)), "mx_selftest_arm_stall")
 
 
 def mx_bounds_check(clear=True):
@@ -331,7 +354,7 @@ def mx_selftest_bounds(buf16, stream=None):
     """Bounds-checked builds: one refused store just past an 8-byte span over
     buf16 (a 16-byte CUDA tensor); returns 0, or -1 in a release build."""
     _dev_tensor(buf16, "buf16", 16)
-    dev = buf16.get_device()
+    dev = _device(buf16)
     with torch.cuda.device(dev):
         rc = _lib().mx_selftest_bounds(_ptr(buf16), _stream(stream, dev))
     if rc < -1:

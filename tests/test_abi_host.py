@@ -210,3 +210,84 @@ def test_c_program_compiles_links_and_calls_host_helpers(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     assert r.stdout.split()[:2] == [str(256 * 8), str((16640 + 512) * 160)]
     assert "current" in r.stdout
+
+
+# ---- the binding's dtype and rank checks ---------------------------------------
+#
+# The C ABI takes untyped pointers, so a float16 tensor handed over as bf16
+# input, or float offsets as int32 group ends, would be read as the wrong bits.
+# The binding refuses them; these checks run before any CUDA call, so CPU
+# tensors reach them here.
+
+def _bf16(*shape):
+    import torch
+    return torch.zeros(shape, dtype=torch.bfloat16)
+
+
+def _u8(n):
+    import torch
+    return torch.zeros(n, dtype=torch.uint8)
+
+
+def test_binding_refuses_float16_input(lib):
+    import torch
+    x = torch.zeros((64, 64), dtype=torch.float16)
+    for fn, args in ((mx.mx_cast_dim0_dim1, (_u8(4096), _u8(4096), _u8(4096), _u8(4096))),
+                     (mx.mx_cast_dim0, (_u8(4096), _u8(4096))),
+                     (mx.mx_cast_dim1, (_u8(4096), _u8(4096))),
+                     (mx.mx_cast_rowwise, (_u8(4096), _bf16(64))),
+                     (mx.mx_cast_tensorwise, (_u8(4096), torch.zeros(1), torch.zeros(1)))):
+        with pytest.raises(TypeError, match="bfloat16"):
+            fn(x, *args)
+    with pytest.raises(TypeError, match="bfloat16"):
+        mx.mx_cast_3d_dim1(torch.zeros((2, 32, 32), dtype=torch.int16), _u8(2048), _u8(4096))
+
+
+def test_binding_refuses_wrong_offset_and_status_dtypes(lib):
+    import torch
+    M, K, G = 256, 64, 2
+    x = _bf16(M, K)
+    n0, n1 = mx.mx_grouped_m_scale_bytes(M, K, G, 0), mx.mx_grouped_m_scale_bytes(M, K, G, 1)
+    good = dict(offs=torch.tensor([100, 256], dtype=torch.int32), q0=_u8(M * K), s0=_u8(n0),
+                r0=torch.zeros(G + 1, dtype=torch.int64), q1=_u8(M * K), s1=_u8(n1),
+                c1=torch.zeros(G + 1, dtype=torch.int64), st=torch.zeros(1, dtype=torch.int32))
+
+    def call(**over):
+        a = dict(good, **over)
+        mx.mx_cast_grouped_m(x, a["offs"], a["q0"], a["s0"], a["r0"], a["q1"], a["s1"],
+                             a["c1"], a["st"])
+
+    with pytest.raises(TypeError, match="int32"):
+        call(offs=torch.tensor([100.0, 256.0], dtype=torch.float32))
+    with pytest.raises(TypeError, match="int32"):
+        call(offs=torch.tensor([100, 256], dtype=torch.int64))
+    with pytest.raises(TypeError, match="int64"):
+        call(r0=torch.zeros(G + 1, dtype=torch.int32).repeat(2))
+    with pytest.raises(TypeError, match="int32"):
+        call(st=torch.zeros(1, dtype=torch.float32))
+    with pytest.raises(TypeError, match="uint8"):
+        call(q0=torch.zeros(M * K, dtype=torch.int8))
+    # correct dtypes on the CPU: refused for not being CUDA tensors
+    with pytest.raises(ValueError, match="CUDA"):
+        call()
+
+
+def test_binding_refuses_wrong_ranks_and_output_dtypes(lib):
+    import torch
+    with pytest.raises(ValueError, match="2 dimensions"):
+        mx.mx_cast_dim0_dim1(_bf16(2, 64, 64), _u8(1), _u8(1), _u8(1), _u8(1))
+    with pytest.raises(ValueError, match="3 dimensions"):
+        mx.mx_cast_3d_dim0(_bf16(64, 64), _u8(1), _u8(1))
+    with pytest.raises(TypeError, match="float32"):
+        mx.mx_cast_tensorwise(_bf16(64), _u8(64), torch.zeros(1, dtype=torch.float64),
+                              torch.zeros(1))
+    with pytest.raises(TypeError, match="bfloat16"):
+        mx.mx_cast_rowwise(_bf16(64, 64), _u8(4096), torch.zeros(64, dtype=torch.float16))
+    with pytest.raises(TypeError, match="bfloat16"):
+        mx.mx_dequant_blocked(_u8(64 * 64).view(64, 64), _u8(512),
+                              torch.zeros((64, 64), dtype=torch.float16))
+    # fp8 and e8m0 views of the byte buffers are accepted by the checks
+    if hasattr(torch, "float8_e4m3fn"):
+        q = torch.zeros((64, 64), dtype=torch.float8_e4m3fn)
+        with pytest.raises(ValueError, match="CUDA"):
+            mx.mx_dequant_blocked(q, _u8(512), _bf16(64, 64))
