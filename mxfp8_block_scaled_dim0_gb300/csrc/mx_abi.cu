@@ -15,6 +15,10 @@ namespace {
 
 thread_local int t_last_cuda = 0;
 
+// Diagnostic stall armed by mx_selftest_arm_stall for this thread's next
+// launch of a kernel with bounded waits (at < 0: none).
+thread_local mx::Stall t_stall = {-1, 0};
+
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 256;   // TMA coordinates are int32
 
 int cuda_fail(int code) {
@@ -163,6 +167,12 @@ int launch_rc(int rc) { return rc ? cuda_fail(rc) : MX_OK; }
 
 }  // namespace
 
+mx::Stall mx::take_stall() {
+  const Stall s = t_stall;
+  t_stall = Stall{-1, 0};
+  return s;
+}
+
 namespace {
 
 // Shared body of the 3D casts: q0 / s0_blk null for dim1 only, q1 / s1_blk
@@ -246,7 +256,10 @@ int mx_watchdog(int clear) {
   if (rc) return cuda_fail(rc);
   rc = mx::read_scaled_watchdog(&w, clear != 0);
   if (rc) return cuda_fail(rc);
-  return v | w;
+  int d = 0;
+  rc = mx::read_dequant_watchdog(&d, clear != 0);
+  if (rc) return cuda_fail(rc);
+  return v | w | d;
 }
 
 int mx_bounds_check(int clear) {
@@ -277,6 +290,12 @@ int mx_selftest_watchdog(int64_t wait_ns, void* stream) {
   if (wait_ns < 1000 || wait_ns > int64_t{10} * 1000 * 1000 * 1000) return MX_ERR_SHAPE;
   return launch_rc(mx::launch_watchdog_selftest(static_cast<uint64_t>(wait_ns),
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int mx_selftest_arm_stall(int64_t at, int64_t wait_ns) {
+  if (at < 0 || wait_ns < 1000 || wait_ns > int64_t{10} * 1000 * 1000 * 1000) return MX_ERR_SHAPE;
+  t_stall = mx::Stall{at, static_cast<uint64_t>(wait_ns)};
+  return MX_OK;
 }
 
 int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, void* q1,
@@ -329,7 +348,16 @@ int mx_dequant_blocked(const void* q, int64_t R, int64_t C, const void* s_blk, v
   if (int rc = check_device({q, s_blk, out})) return rc;
   int sms = 0;
   if (int rc = current_sm_count(&sms)) return rc;
-  return launch_rc(mx::launch_dequant_blocked(static_cast<const uint8_t*>(q), R, C,
+  mx::DqMaps maps;
+  if (C >= mx::kDqTmaMinCols) {
+    if (int rc = encode_2d(&maps.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, C, R, C, 128, 128,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+      return rc;
+    if (int rc = encode_2d(&maps.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, C, R, 2 * C, 64, 128,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE))
+      return rc;
+  }
+  return launch_rc(mx::launch_dequant_blocked(&maps, static_cast<const uint8_t*>(q), R, C,
                                               static_cast<const uint8_t*>(s_blk),
                                               static_cast<uint16_t*>(out), sms,
                                               static_cast<cudaStream_t>(stream)));

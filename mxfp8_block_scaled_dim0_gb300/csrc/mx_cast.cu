@@ -36,7 +36,9 @@
 // output staging buffers.  More loads in flight (4-5 stages) slowed the
 // kernel by ~12%: outstanding writes, not reads, limit the mixed stream.
 // Every wait is bounded (see mbar_wait); on time-out the CTA raises an abort
-// flag, stops, drains its own bulk copies and reports through a device word.
+// flag, stops, lets its own copies in flight land (the TMA loads into its
+// input ring and the bulk stores out of its staging) and reports through a
+// device word.
 #include <cuda_runtime.h>
 
 #include "mx_common.cuh"
@@ -73,7 +75,7 @@ constexpr int kOffCarry = kOffS1 + kStaging * kScaleTile;   // grouped: 128 x 16
 constexpr int kOffGTab = kOffCarry + kTile * 16;
 constexpr int kGTabBytes = ((2 * kMaxSmemGroups + 1) * 4 + 127) / 128 * 128;
 constexpr int kOffBar = kOffGTab + kGTabBytes;
-constexpr int kNumBars = 2 * kStages + 2 * kStaging;
+constexpr int kNumBars = 2 * kStages + 2 * kStaging + 1;   // + the diagnostic stall barrier
 constexpr int kQ1GroupBoxRows = static_cast<int>(kQ1BoxRowsGrouped);  // grouped: per-warp q1 box rows
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffFlag + 16;   // flag: abort (+0), bad group offsets (+4)
@@ -152,6 +154,10 @@ struct Params {
                             // whole 128-byte tiles may leave by TMA
   // output buffers, for the bounds-checked build's store checks
   Span sp_q0, sp_q1, sp_s0, sp_s1, sp_ro, sp_co, sp_st;
+  // diagnostic stall (mx_kernels.h): CTA 0's compute warps at run position
+  // stall_at, -1 in normal use
+  int64_t stall_at;
+  uint64_t stall_ns;
 };
 
 // Group table of the grouped mode: tr[g] = padded tile-rows before group g
@@ -292,6 +298,14 @@ __device__ __forceinline__ Tile role_tile(const Params& p, const GroupTab& tab, 
 
 // ---- compute units ----------------------------------------------------------
 
+// Sixteen e4m3 NaN bytes (0x7F), the elements of a block whose scale is the
+// e8m0 NaN (0xFF): the product with a NaN multiplier converts to an e4m3 NaN
+// already, but with whichever sign the NaN carries, so the bytes are set
+// outright.
+__device__ __forceinline__ uint4 nan_e4m3x16() {
+  return make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+}
+
 // dim0 half-block unit (16 elements), stored straight to q0.  In warp step
 // with first row R0 (even), lane l takes row R0 + ((l >> 2) & 1) + 2*(l >> 4),
 // 64-column half `box` = (l >> 3) & 1 and half-block hq = l & 3 of that half:
@@ -328,6 +342,7 @@ __device__ __forceinline__ void dim0_half_unit(const uint8_t* in, uint8_t* sc0, 
   o.y = e4m3x4(bf_lo(v0.z), bf_hi(v0.z), bf_lo(v0.w), bf_hi(v0.w), m);
   o.z = e4m3x4(bf_lo(v1.x), bf_hi(v1.x), bf_lo(v1.y), bf_hi(v1.y), m);
   o.w = e4m3x4(bf_lo(v1.z), bf_hi(v1.z), bf_lo(v1.w), bf_hi(v1.w), m);
+  if (sbyte == 0xFFu) o = nan_e4m3x16();          // Inf / NaN block: every element NaN
   const int64_t gr = static_cast<int64_t>(m0) + row;
   const int64_t gc = static_cast<int64_t>(k0) + 64 * box + 16 * hq;
   if (row < rows && gr < M && gc < K && in_span(p.sp_q0, q0 + gr * K + gc, 16))
@@ -395,6 +410,8 @@ __device__ __forceinline__ uint32_t dim1_unit(const uint8_t* in, uint8_t* q1s, u
   o0.z = MX_COL4_HI(w, 8, mo);  o0.w = MX_COL4_HI(w, 12, mo);
   o1.x = MX_COL4_HI(w, 16, mo); o1.y = MX_COL4_HI(w, 20, mo);
   o1.z = MX_COL4_HI(w, 24, mo); o1.w = MX_COL4_HI(w, 28, mo);
+  if (se == 0xFFu) e0 = e1 = nan_e4m3x16();       // Inf / NaN block: every element NaN
+  if (so == 0xFFu) o0 = o1 = nan_e4m3x16();
   const int sw = p & 7;
   uint8_t* de = q1s + p * 128;
   uint8_t* dodd = q1s + kQ1Half + p * 128;
@@ -578,6 +595,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   uint64_t* empty = bars + kStages;           // [kStages] compute done reading
   uint64_t* sfull = bars + 2 * kStages;       // [kStaging] staging written
   uint64_t* sempty = sfull + kStaging;        // [kStaging] staging drained
+  uint64_t* stall_bar = sempty + kStaging;    // diagnostic: never completed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
 
   const int warp = threadIdx.x >> 5;
@@ -676,12 +694,14 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       mbar_init(&sfull[o], kComputeWarps);
       mbar_init(&sempty[o], store_warps(kMode));
     }
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
 
+  int64_t issued = 0;                         // producer lane: TMA loads issued
   if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tmap(&tm_x);
@@ -697,6 +717,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
         mbar_arrive_expect_tx(&full[s], kInBytes);
         tma_load_2d(dst, &tm_x, T.k0, T.m0, &full[s]);
         tma_load_2d(dst + kHalfBytes, &tm_x, T.k0 + 64, T.m0, &full[s]);
+        issued = static_cast<int64_t>(it) + 1;
       }
     }
     __syncwarp();
@@ -788,6 +809,11 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
       const int o = static_cast<int>(it % kStaging);
       const uint32_t oph = static_cast<uint32_t>((it / kStaging) & 1);
+      if (static_cast<int64_t>(it) == p.stall_at && blockIdx.x == 0) {
+        // Diagnostic (armed from the host only): a wait that runs out.
+        mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);
+        break;
+      }
       bool ok = mbar_wait(&full[s], ph, abort_flag);
       ok = ok && mbar_wait(&sempty[o], oph ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -864,7 +890,17 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   }
 
   __syncthreads();
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_watchdog, 1);
+  if (*abort_flag && warp == kProducerWarp && lane == 0) {
+    // A role gave up: TMA loads issued into the input ring may never have
+    // been consumed.  Let each stage's last one land (bounded) before the CTA
+    // exits and its shared memory is reused, then report.
+    for (int s = 0; s < kStages; ++s) {
+      if (issued <= s) break;
+      const int64_t last = s + (issued - 1 - s) / kStages * kStages;   // last load into s
+      mbar_drain(&full[s], static_cast<uint32_t>((last / kStages) & 1));
+    }
+    atomicOr(&g_watchdog, 1);
+  }
 }
 
 }  // namespace
@@ -918,6 +954,9 @@ int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s
   const bool dim0 = q0 != nullptr;
   const bool dim1 = s1 != nullptr;
   Params prm = {};
+  const Stall stall = take_stall();
+  prm.stall_at = stall.at;
+  prm.stall_ns = stall.ns;
   prm.q0 = static_cast<uint8_t*>(q0);
   prm.M = M;
   prm.K = K;
@@ -941,6 +980,9 @@ int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, v
   const bool dim0 = q0 != nullptr;
   const bool dim1 = s1 != nullptr;
   Params prm = {};
+  const Stall stall = take_stall();
+  prm.stall_at = stall.at;
+  prm.stall_ns = stall.ns;
   prm.q0 = static_cast<uint8_t*>(q0);
   prm.s0 = static_cast<uint8_t*>(s0);
   prm.kb4 = static_cast<int32_t>(((K / 32) + 3) / 4 * 4);
@@ -970,6 +1012,9 @@ int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_
                         void* q0, void* q1, void* s0, int64_t* row_offs, int64_t* col_offs,
                         void* s1, int32_t* status, int num_sms, cudaStream_t stream) {
   Params prm = {};
+  const Stall stall = take_stall();
+  prm.stall_at = stall.at;
+  prm.stall_ns = stall.ns;
   prm.q0 = static_cast<uint8_t*>(q0);
   prm.M = M;
   prm.K = K;

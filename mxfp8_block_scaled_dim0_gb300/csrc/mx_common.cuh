@@ -91,6 +91,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Wait, regardless of the abort flag, for the phase of parity `parity` to
+// complete, giving up after limit_ns.  Used on the way out of a CTA that gave
+// up: asynchronous copies it issued into its own shared memory must land
+// before the CTA exits.  Returns false if the limit passed.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity,
+                                           uint64_t limit_ns = kWaitLimitNs) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
 // ---- TMA (tensor) and bulk copies -------------------------------------------
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -116,6 +128,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t x, in
                    "l"(reinterpret_cast<uint64_t>(m)),
                "r"(x), "r"(y), "r"(smem_u32(smem_src))
                : "memory");
+}
+
+// Plain bulk copy global -> smem completing on `bar` (bytes counted as
+// transaction bytes); both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Plain bulk copy smem -> global; both addresses 16-byte aligned, bytes % 16 == 0.

@@ -142,10 +142,217 @@ __global__ void __launch_bounds__(kDqThreads) dequant_blocked_kernel(const DqPar
   }
 }
 
+// ---- tiled kernel (rows of 128 values or more) --------------------------------
+//
+// Persistent, one CTA per SM, warp-specialised like the cast kernels: a
+// producer warp brings each 128 x 128 tile of q (16 KB, TMA, 128B swizzle)
+// and the one 512-byte blocked scale tile that covers it (a 128 x 128 tile of
+// q has exactly one: 128 rows x 4 scale columns) into a ring of stages; eight
+// compute warps convert the tile into a bf16 staging tile (two 64-column
+// halves, 128B swizzle); a store warp writes each staging tile out with two
+// TMA tensor stores.  Tiles past the matrix's edge are zero-filled on load and
+// clipped on store by the tensor maps, so any R and any C % 32 == 0 works.
+// Every wait is bounded; on time-out the CTA stops, lets its copies in flight
+// land and reports through g_dequant_watchdog.
+constexpr int kDqTile = 128;
+constexpr int kDqInBytes = kDqTile * kDqTile;       // e4m3 tile
+constexpr int kDqScaleBytes = 512;                  // one blocked scale tile
+constexpr int kDqOutHalf = kDqTile * 128;           // 64 bf16 columns x 128 rows
+constexpr int kDqOutBytes = 2 * kDqOutHalf;
+constexpr int kDqStages = 4;                        // input ring depth
+constexpr int kDqStaging = 4;                       // output staging buffers
+constexpr int kDqComputeWarps = 8;
+constexpr int kDqProducerWarp = kDqComputeWarps;
+constexpr int kDqStoreWarp = kDqComputeWarps + 1;
+constexpr int kDqTmaThreads = (kDqComputeWarps + 2) * 32;
+constexpr int kDqOffIn = 0;
+constexpr int kDqOffOut = kDqOffIn + kDqStages * kDqInBytes;
+constexpr int kDqOffScale = kDqOffOut + kDqStaging * kDqOutBytes;
+constexpr int kDqOffBar = kDqOffScale + kDqStages * kDqScaleBytes;
+constexpr int kDqNumBars = 2 * kDqStages + 2 * kDqStaging + 1;   // + the diagnostic stall
+constexpr int kDqOffFlag = kDqOffBar + kDqNumBars * 8;
+constexpr int kDqSmemBytes = kDqOffFlag + 16 + 1024;             // + alignment slack
+static_assert(kDqSmemBytes <= 227 * 1024, "shared memory budget");
+
+__device__ int g_dequant_watchdog = 0;
+
+struct DqTmaParams {
+  const uint8_t* s;      // blocked scales
+  int64_t C;             // columns
+  int64_t n_tc;          // tile columns, ceil(C / 128)
+  int64_t n_tiles;
+  int64_t s_tiles_row;   // blocked scale tiles per 128-row band, ceil4(C / 32) / 4
+  int64_t stall_at;      // diagnostic stall (mx_kernels.h), -1 in normal use
+  uint64_t stall_ns;
+};
+
+__global__ void __launch_bounds__(kDqTmaThreads, 1)
+    dequant_tma_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_out, const DqTmaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDqOffBar);   // [kDqStages] tile landed
+  uint64_t* empty = full + kDqStages;                                // [kDqStages] tile read
+  uint64_t* sfull = empty + kDqStages;                               // [kDqStaging] staged
+  uint64_t* sempty = sfull + kDqStaging;                             // [kDqStaging] drained
+  uint64_t* stall_bar = sempty + kDqStaging;                         // never completed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kDqOffFlag);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDqStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDqComputeWarps);
+    }
+    for (int o = 0; o < kDqStaging; ++o) {
+      mbar_init(&sfull[o], kDqComputeWarps);
+      mbar_init(&sempty[o], 1);
+    }
+    mbar_init(stall_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // Programmatic dependent launch: the barriers above touch no global memory;
+  // every global access waits for the earlier grids.
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+
+  int64_t issued = 0;   // producer lane: tiles whose loads were issued
+  if (warp == kDqProducerWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      int64_t it = 0;
+      for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
+        const int s = static_cast<int>(it % kDqStages);
+        if (!mbar_wait(&empty[s], static_cast<uint32_t>(((it / kDqStages) & 1) ^ 1), abort_flag))
+          break;
+        const int64_t tr = t / p.n_tc, tc = t - tr * p.n_tc;
+        mbar_arrive_expect_tx(&full[s], kDqInBytes + kDqScaleBytes);
+        tma_load_2d(smem + kDqOffIn + s * kDqInBytes, &tm_q, static_cast<int32_t>(tc * kDqTile),
+                    static_cast<int32_t>(tr * kDqTile), &full[s]);
+        bulk_load(smem + kDqOffScale + s * kDqScaleBytes,
+                  p.s + (tr * p.s_tiles_row + tc) * kDqScaleBytes, kDqScaleBytes, &full[s]);
+        issued = it + 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kDqStoreWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tm_out);
+      int64_t it = 0;
+      for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
+        const int o = static_cast<int>(it % kDqStaging);
+        if (!mbar_wait(&sfull[o], static_cast<uint32_t>((it / kDqStaging) & 1), abort_flag)) break;
+        const int64_t tr = t / p.n_tc, tc = t - tr * p.n_tc;
+        const uint8_t* stg = smem + kDqOffOut + o * kDqOutBytes;
+        const int32_t x0 = static_cast<int32_t>(tc * kDqTile), y0 = static_cast<int32_t>(tr * kDqTile);
+        tma_store_2d(&tm_out, x0, y0, stg);
+        // (the right half of the last tile column may lie wholly past the
+        // matrix when C % 128 != 0: no store starts outside it)
+        if (x0 + 64 < p.C) tma_store_2d(&tm_out, x0 + 64, y0, stg + kDqOutHalf);
+        // Keep the newest bulk group in flight: the previous tile's staging
+        // buffer is released once its own group has been read.
+        bulk_commit();
+        bulk_wait_read<1>();
+        if (it > 0) mbar_arrive(&sempty[static_cast<int>((it - 1) % kDqStaging)]);
+      }
+      bulk_wait<0>();
+    }
+    __syncwarp();
+  } else {
+    // Compute warp w converts rows 16w .. 16w + 15, two per step: lane l takes
+    // row 16w + 2k + (l >> 4), 64-column half h = (l >> 3) & 1 and the eight
+    // values of output chunk j = l & 7 of that half.  Its 8 input bytes lie in
+    // input chunk 4h + (j >> 1); each half-warp reads one whole 128-byte row of
+    // q and each 8-lane phase writes eight distinct chunks of one staging row
+    // (both conflict-free under the swizzle).
+    const int h = (lane >> 3) & 1;
+    const int j = lane & 7;
+    const int cin = 4 * h + (j >> 1);
+    const int c4 = 2 * h + (j >> 2);                 // scale column within the tile
+    int64_t it = 0;
+    for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
+      const int s = static_cast<int>(it % kDqStages);
+      const int o = static_cast<int>(it % kDqStaging);
+      if (it == p.stall_at && blockIdx.x == 0) {
+        // Diagnostic (armed from the host only): a wait that runs out.
+        mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);
+        break;
+      }
+      bool ok = mbar_wait(&full[s], static_cast<uint32_t>((it / kDqStages) & 1), abort_flag);
+      ok = ok && mbar_wait(&sempty[o], static_cast<uint32_t>(((it / kDqStaging) & 1) ^ 1),
+                           abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint8_t* in = smem + kDqOffIn + s * kDqInBytes;
+      const uint8_t* sc = smem + kDqOffScale + s * kDqScaleBytes;
+      uint8_t* stg = smem + kDqOffOut + o * kDqOutBytes + h * kDqOutHalf;
+#pragma unroll 4
+      for (int k = 0; k < 8; ++k) {
+        const int r = 16 * warp + 2 * k + (lane >> 4);
+        const int sw = r & 7;
+        const uint2 v =
+            *reinterpret_cast<const uint2*>(in + r * 128 + ((cin ^ sw) << 4) + 8 * (j & 1));
+        const uint32_t sb = sc[blocked_in_tile(r, c4)];
+        *reinterpret_cast<uint4*>(stg + r * 128 + ((j ^ sw) << 4)) = dequant8(v, e8m0_value(sb));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      fence_proxy_async_smem();                      // staging writes -> TMA store reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfull[o]);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag && warp == kDqProducerWarp && lane == 0) {
+    // A role gave up: let each stage's last issued load land (bounded) before
+    // the CTA exits, then report.
+    for (int s = 0; s < kDqStages; ++s) {
+      if (issued <= s) break;
+      const int64_t last = s + (issued - 1 - s) / kDqStages * kDqStages;
+      mbar_drain(&full[s], static_cast<uint32_t>((last / kDqStages) & 1));
+    }
+    atomicOr(&g_dequant_watchdog, 1);
+  }
+}
+
 }  // namespace
 
-int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t* s_blk,
-                           uint16_t* out, int num_sms, cudaStream_t stream) {
+int launch_dequant_blocked(const DqMaps* maps, const uint8_t* q, int64_t R, int64_t C,
+                           const uint8_t* s_blk, uint16_t* out, int num_sms, cudaStream_t stream) {
+  if (C >= kDqTmaMinCols) {
+    DqTmaParams p = {};
+    p.s = s_blk;
+    p.C = C;
+    p.n_tc = (C + kDqTile - 1) / kDqTile;
+    p.n_tiles = (R + kDqTile - 1) / kDqTile * p.n_tc;
+    p.s_tiles_row = ((C / 32) + 3) / 4;
+    const Stall stall = take_stall();
+    p.stall_at = stall.at;
+    p.stall_ns = stall.ns;
+    static DeviceCache attr_cache;
+    const int attr = attr_cache.get([] {
+      return static_cast<int>(cudaFuncSetAttribute(
+          dequant_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmemBytes));
+    });
+    if (attr != 0) return attr;
+    const int grid = static_cast<int>(p.n_tiles < num_sms ? p.n_tiles : num_sms);
+    if (grid <= 0) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDqTmaThreads);
+    cfg.dynamicSmemBytes = kDqSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr_pdl[1];
+    attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_pdl;
+    cfg.numAttrs = 1;
+    return static_cast<int>(cudaLaunchKernelEx(&cfg, dequant_tma_kernel, maps->q, maps->out, p));
+  }
   DqParams p = {};
   p.q = q;
   p.s = s_blk;
@@ -193,5 +400,18 @@ int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t
 }
 
 int out_of_bounds_dequant(bool clear) { return read_out_of_bounds(clear); }
+
+int read_dequant_watchdog(int* out, bool clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_dequant_watchdog, sizeof(int));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  if (clear && v) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_dequant_watchdog, &z, sizeof(int));
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
+  *out = v;
+  return 0;
+}
 
 }  // namespace mx

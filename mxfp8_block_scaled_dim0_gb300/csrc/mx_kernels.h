@@ -45,6 +45,18 @@ struct CastMaps {
   CUtensorMap q1o;
 };
 
+// Diagnostic stall, armed from the host (mx_selftest_arm_stall) for the next
+// cast or bulk-staged rowwise launch of the arming thread: CTA 0's compute
+// threads wait, at their `at`-th tile (or step), on a barrier that nothing
+// completes, for at most `ns` nanoseconds, so that the wait runs out and the
+// CTA winds down through its abort path.  at < 0: none (normal use).
+struct Stall {
+  int64_t at;
+  uint64_t ns;
+};
+// The armed stall, disarmed by the call (mx_abi.cu).
+Stall take_stall();
+
 constexpr unsigned kQ1BoxRowsFused = 64;
 constexpr unsigned kQ1BoxRowsGrouped = 16;
 
@@ -67,9 +79,18 @@ int launch_cast_tensorwise(const uint16_t* x, int64_t n, uint8_t* q, float* scal
                            int num_sms, cudaStream_t stream);
 int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uint16_t* scale,
                         int num_sms, cudaStream_t stream);
-// MX dequantisation (mx_dequant.cu).
-int launch_dequant_blocked(const uint8_t* q, int64_t R, int64_t C, const uint8_t* s_blk,
-                           uint16_t* out, int num_sms, cudaStream_t stream);
+// MX dequantisation (mx_dequant.cu).  Rows of at least kDqTmaMinCols values
+// take the tiled kernel, which needs the two TMA descriptors (q: e4m3 bytes,
+// boxes of 128 x 128, 128B swizzle; out: bf16, boxes of 64 x 128, 128B
+// swizzle); shorter rows take the thread-store kernel, which needs none.
+struct DqMaps {
+  CUtensorMap q;
+  CUtensorMap out;
+};
+constexpr int64_t kDqTmaMinCols = 128;
+int launch_dequant_blocked(const DqMaps* maps, const uint8_t* q, int64_t R, int64_t C,
+                           const uint8_t* s_blk, uint16_t* out, int num_sms, cudaStream_t stream);
+int read_dequant_watchdog(int* out, bool clear);
 // G <= kMaxSmemGroups: one kernel builds the group table itself; larger G:
 // group_offsets_kernel first, then the cast kernel as its programmatic
 // dependent.

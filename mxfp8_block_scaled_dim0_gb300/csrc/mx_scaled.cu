@@ -269,12 +269,14 @@ __device__ int g_scaled_watchdog = 0;
 __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* x, int64_t M,
                                                                 int64_t K, int t_log2, int stages,
                                                                 uint8_t* q, uint16_t* scale,
-                                                                Span sp_q, Span sp_scale) {
+                                                                Span sp_q, Span sp_scale,
+                                                                int64_t stall_at, uint64_t stall_ns) {
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint32_t red[kThreads / 32];
   __shared__ __align__(8) uint64_t full[8];
+  __shared__ __align__(8) uint64_t stall_bar;   // diagnostic: never completed
   __shared__ int abort_flag;
   const int T = 1 << t_log2;
   const int groups = kThreads >> t_log2;
@@ -301,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < stages; ++st) mbar_init(&full[st], 1);
+    mbar_init(&stall_bar, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -312,6 +315,13 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
   int64_t i = 0;
   for (; i < n_steps; ++i) {
     const int st = static_cast<int>(i % stages);
+    if (i == stall_at && blockIdx.x == 0) {
+      // Diagnostic (armed from the host only): a wait that runs out; every
+      // thread of the CTA takes it, and the abort path below lets the copies
+      // in flight land.
+      mbar_wait(&stall_bar, 0u, &abort_flag, stall_ns);
+      break;
+    }
     const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1), &abort_flag);
     if (!__syncthreads_and(ok)) break;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * groups + i * step_rows + g;
@@ -455,8 +465,9 @@ int launch_cast_rowwise(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, uin
     attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr_pdl;
     cfg.numAttrs = 1;
+    const Stall stall = take_stall();
     return static_cast<int>(cudaLaunchKernelEx(&cfg, rowwise_bulk_kernel, x, M, K, t_log2, stages, q,
-                                               scale, sp_q, sp_scale));
+                                               scale, sp_q, sp_scale, stall.at, stall.ns));
   }
   static DeviceCache occ;
   const int per = occ.get([] { return wave(rowwise_kernel, 1); });

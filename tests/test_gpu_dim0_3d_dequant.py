@@ -89,7 +89,8 @@ def test_dim0_only_matches_oracle(M, K):
 
 def test_dim0_only_equals_fused_dim0_full_size():
     """At 16384^2 the dim0-only launch writes the same q0 / s0 bytes as the
-    fused launch (checked against the oracle on sampled rows)."""
+    fused launch, which test_gpu_full_size.py compares with the oracle byte
+    for byte; sampled rows are also checked against the oracle here."""
     x = W.make("square16384_weight", device="cuda")["x"]
     M, K = x.shape
     q0, s0 = mx.cast_dim0(x)
@@ -145,30 +146,6 @@ def test_3d_fused_matches_oracle(E, N, K):
     assert_bytes_equal(to_np(s1), os1, "s1 per expert")
 
 
-def test_3d_fused_expert_workload_sampled():
-    """The (16, 8192, 5120) expert weights through the fused 3D launch: q1 and
-    s1 equal the dim1-only launch, q0 and s0 the dim0-only launch; sampled
-    rows of q0 and every third expert's sampled scale rows against the
-    oracle."""
-    w = W.make("experts16x8192x5120", device="cuda")["x"]
-    E, N, K = w.shape
-    q0, s0, q1, s1 = mx.cast_3d_dim0_dim1(w)
-    r1, rs1 = mx.cast_3d_dim1(w)
-    r0, rs0 = mx.cast_3d_dim0(w)
-    torch.cuda.synchronize()
-    assert torch.equal(q1, r1) and torch.equal(s1, rs1)
-    assert torch.equal(q0, r0) and torch.equal(s0, rs0)
-    del r1, rs1, r0, rs0
-    per = mx.mx_blocked_bytes(N, K // 32)
-    g = torch.Generator().manual_seed(4)
-    for e in range(0, E, 3):
-        rows = torch.randperm(N, generator=g)[:24].sort().values
-        oq, os_ = oracle.cast_dim0(W.bf16_bits(w[e][rows.cuda()]))
-        assert_bytes_equal(to_np(q0[e][rows.cuda()]), oq, "q0 expert %d" % e)
-        plain = oracle.from_blocked(to_np(s0[e * per:(e + 1) * per]), N, K // 32)
-        assert_bytes_equal(plain[rows.numpy()], os_, "s0 expert %d" % e)
-
-
 # ---- dequantisation ---------------------------------------------------------------
 
 def _golden_dequant():
@@ -218,6 +195,20 @@ def test_dequant_every_element_every_scale():
     assert_bf16_equal(_gpu_dequant(q, s_blk), oracle.dequant_blocked(q, s_blk), "all pairs")
 
 
+def test_dequant_every_element_every_scale_tiled():
+    """The same 65,536 (element, scale) pairs laid out in rows of 128 values,
+    the tiled kernel's path: block b (row b // 4, scale column b % 4) has scale
+    byte b % 256 and elements (32 (b // 256) + i) % 256, so every scale byte
+    meets every element byte four times."""
+    R, C = 2048, 128
+    b = np.arange(R * C // 32)
+    s = (b % 256).astype(np.uint8).reshape(R, C // 32)
+    q = ((32 * (b[:, None] // 256) + np.arange(32)[None, :]) % 256).astype(np.uint8)
+    q = q.reshape(R, C)
+    s_blk = oracle.to_blocked(s)
+    assert_bf16_equal(_gpu_dequant(q, s_blk), oracle.dequant_blocked(q, s_blk), "all pairs tiled")
+
+
 @pytest.mark.parametrize("M,K", [(32, 32), (160, 96), (544, 1056), (96, 4128), (256, 2048),
                                  (1024, 160)])
 def test_dequant_of_cast_matches_oracle(M, K):
@@ -233,7 +224,11 @@ def test_dequant_of_cast_matches_oracle(M, K):
     assert_bf16_equal(bf16_np(d1), oracle.dequant_blocked(oq1, os1), "dequant dim1")
 
 
-@pytest.mark.parametrize("R,C", [(1, 32), (77, 96), (3, 8192)])
+# Rows shorter than 128 values take the thread-store kernel, longer ones the
+# tiled kernel, whose last tile column may hold only 32 .. 96 columns (C % 128
+# != 0) and whose last tile row may be partial.
+@pytest.mark.parametrize("R,C", [(1, 32), (77, 96), (3, 8192), (1, 128), (77, 160), (129, 4128),
+                                 (300, 224), (130, 1056)])
 def test_dequant_ragged_shapes(R, C):
     rng = np.random.default_rng(R * 7 + C)
     q = rng.integers(0, 256, size=(R, C), dtype=np.uint8)

@@ -1,11 +1,10 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle, byte
 for byte (fp8 data, e8m0 scales, padded blocked buffers, group offsets).
 
-Sizes span several 128x128 tiles with ragged tails; the full-size workloads
-(the ones the benchmark times, in the same launch configuration) are checked
-on sampled rows / columns the oracle computes on their own, plus properties
-that hold at any size.  Every expected value comes from the oracle run on the
-same seeded input in the same test.
+Sizes span several 128x128 tiles with ragged tails, up to the grouped MoE
+workload (16640 x 5120, 4 groups) compared in full; the two largest workloads
+are compared byte for byte in test_gpu_full_size.py.  Every expected value
+comes from the oracle run on the same seeded input in the same test.
 """
 import numpy as np
 import pytest
@@ -143,24 +142,27 @@ def test_edge_values(golden_blocks):
 
 
 def test_nan_inf_blocks_reading():
-    """Not pinned by the pages (no workload holds NaN/Inf): a block with NaN or
-    Inf gets scale byte 0xFF and every element an e4m3 NaN (0x7F or 0xFF);
-    all other blocks are unaffected."""
+    """Not pinned by the pages (no workload holds NaN/Inf): a block with NaN,
+    -NaN, Inf or -Inf gets scale byte 0xFF and every element the e4m3 NaN
+    0x7F; all other blocks are unaffected.  Every byte equals the oracle's,
+    in both directions and through the grouped kernel."""
     M, K = 64, 64
-    x = W.normal((M, K), 5)
-    xn = x.clone()
-    xn[3, 40] = float("nan")
-    xn[40, 5] = float("inf")
+    bits = W.bf16_bits(W.normal((M, K), 5)).copy()
+    bits[3, 40] = 0x7FC0          # NaN
+    bits[40, 5] = 0x7F80          # +Inf
+    bits[50, 60] = 0xFF80         # -Inf
+    bits[20, 10] = 0xFFC1         # a NaN with the sign bit set and a payload
+    xn = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     got = run_fused(xn.cuda())
     bits = W.bf16_bits(xn)
     q0, s0, q1, s1 = oracle.cast_dim0_dim1_blocked(bits)
     assert_bytes_equal(got["s0"], s0, "s0")
     assert_bytes_equal(got["s1"], s1, "s1")
-    for name, ref in (("q0", q0), ("q1", q1)):
-        g = got[name]
-        nan = (ref & 0x7F) == 0x7F
-        assert np.all((g[nan] & 0x7F) == 0x7F), name
-        assert_bytes_equal(g[~nan], ref[~nan], name)
+    assert np.count_nonzero(oracle.from_blocked(s0, M, K // 32) == 0xFF) == 4
+    assert_bytes_equal(got["q0"], q0, "q0")
+    assert_bytes_equal(got["q1"], q1, "q1")
+    assert np.count_nonzero(q0 == 0x7F) == 4 * 32   # four NaN blocks per direction
+    compare_grouped(xn, [17, 64])
 
 
 def test_repeat_calls_identical_and_stream_ordered():
@@ -172,39 +174,6 @@ def test_repeat_calls_identical_and_stream_ordered():
     s.synchronize()
     for u, v in zip(a, b):
         assert torch.equal(u, v)
-
-
-# ---- full size (the benchmarked workload) --------------------------------------
-
-def test_full_size_weight_sampled_and_transpose_property():
-    """16384 x 16384 weight-like matrix, the benchmark's launch: sampled rows
-    (dim0) and sampled columns (dim1) against the oracle, and the property
-    dim1(X) == dim0(X^T) between two full-size GPU calls."""
-    x = W.make("square16384_weight", device="cuda")["x"]
-    M, K = x.shape
-    q0, s0, q1, s1 = mx.cast_dim0_dim1(x)
-    torch.cuda.synchronize()
-    g = torch.Generator().manual_seed(5)
-    rows = torch.randperm(M, generator=g)[:96].sort().values
-    cols = torch.randperm(K, generator=g)[:96].sort().values
-    # dim0 of sampled rows (rows are independent under dim0)
-    xr = W.bf16_bits(x[rows.cuda()])
-    oq0, os0 = oracle.cast_dim0(xr)
-    assert_bytes_equal(to_np(q0[rows.cuda()]), oq0, "q0 rows")
-    s0_plain = oracle.from_blocked(to_np(s0), M, K // 32)
-    assert_bytes_equal(s0_plain[rows.numpy()], os0, "s0 rows")
-    # dim1 of sampled columns (columns are independent under dim1)
-    xc = W.bf16_bits(x[:, cols.cuda()])
-    oq1, os1 = oracle.cast_dim1(xc)
-    assert_bytes_equal(to_np(q1[cols.cuda()]), oq1, "q1 rows")
-    s1_plain = oracle.from_blocked(to_np(s1), K, M // 32)
-    assert_bytes_equal(s1_plain[cols.numpy()], os1, "s1 rows")
-    # property at full size: the dim1 outputs equal the dim0 outputs of X^T
-    xt = x.t().contiguous()
-    del q0, s0
-    t0, ts0, _, _ = mx.cast_dim0_dim1(xt)
-    assert torch.equal(t0, q1)
-    assert torch.equal(ts0, s1)
 
 
 # ---- standalone blocked layout ---------------------------------------------------
@@ -360,24 +329,6 @@ def test_3d_matches_oracle(E, N, K):
     oq1, os1 = oracle.cast_3d_dim1(W.bf16_bits(w))
     assert_bytes_equal(to_np(q1).reshape(K, E * N), oq1, "q1")
     assert_bytes_equal(to_np(s1), os1, "s1 per expert")
-
-
-def test_3d_expert_workload_sampled():
-    """The (16, 8192, 5120) expert weights: every expert's scales and sampled
-    q1 rows against the oracle on sampled columns of each expert."""
-    w = W.make("experts16x8192x5120", device="cuda")["x"]
-    E, N, K = w.shape
-    q1, s1 = mx.cast_3d_dim1(w)
-    torch.cuda.synchronize()
-    per = mx.mx_blocked_bytes(K, N // 32)
-    g = torch.Generator().manual_seed(3)
-    cols = torch.randperm(K, generator=g)[:40].sort().values
-    for e in range(0, E, 5):
-        xe = W.bf16_bits(w[e][:, cols.cuda()])          # (N, 40): columns of expert e
-        oq, os_ = oracle.cast_dim1(xe)
-        assert_bytes_equal(to_np(q1[cols.cuda(), e * N:(e + 1) * N]), oq, "q1 expert %d" % e)
-        plain = oracle.from_blocked(to_np(s1[e * per:(e + 1) * per]), K, N // 32)
-        assert_bytes_equal(plain[cols.numpy()], os_, "s1 expert %d" % e)
 
 
 def test_cuda_graph_capture_replays_identically():
