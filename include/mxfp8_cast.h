@@ -260,9 +260,9 @@ int mx_selftest_watchdog(int64_t wait_ns, void* stream);
  * whose waits are bounded (the cast kernels of mx_cast_dim0_dim1,
  * mx_cast_dim0, mx_cast_dim1, mx_cast_grouped_m and the 3D casts; the
  * bulk-staged kernel of mx_cast_rowwise, used for K <= 24576; the tiled
- * kernel of mx_dequant_blocked, used for C >= 128).  In that launch
- * the compute threads of CTA 0, at their `at`-th tile (rowwise: step), wait
- * on a barrier that nothing completes, for at most `wait_ns` nanoseconds
+ * kernel of mx_dequant_blocked, used for C >= 1024).  In that launch the
+ * thread of CTA 0 that issues its loads waits, at its `at`-th tile (rowwise:
+ * step), on a barrier that nothing completes, for at most `wait_ns` nanoseconds
  * (1e3 .. 1e10).  The wait gives up, the CTA stops every role, lets the
  * copies it has in flight land, sets the word read by mx_watchdog(), and the
  * kernel returns normally: the abort path of a real cast, exercised without

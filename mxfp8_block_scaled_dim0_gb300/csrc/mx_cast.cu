@@ -154,7 +154,7 @@ struct Params {
                             // whole 128-byte tiles may leave by TMA
   // output buffers, for the bounds-checked build's store checks
   Span sp_q0, sp_q1, sp_s0, sp_s1, sp_ro, sp_co, sp_st;
-  // diagnostic stall (mx_kernels.h): CTA 0's compute warps at run position
+  // diagnostic stall (mx_kernels.h): CTA 0's producer at run position
   // stall_at, -1 in normal use
   int64_t stall_at;
   uint64_t stall_ns;
@@ -234,13 +234,24 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, i
 // Grouped mode: tiles are ordered by group, then K tile, then M tile within
 // the group, so that a CTA's contiguous run of tiles walks down one column
 // strip of a group (this lets q1 rows be written in whole 16-byte chunks, see
-// copy_out_q1).  Every role walks its run in order, so it keeps a cursor
-// (group, K tile, M tile) that advances one tile at a time: one search of the
-// group table per run instead of a search and a division per tile (the search
-// alone cost about 2 us per doubling of the group count at 16640 x 5120).
+// copy_out_q1).  A group much taller than a run is cut into bands of tile-rows
+// as tall as a run (band, then K tile, then M tile within the band): the 152
+// runs in flight then cover whole tile-rows of X instead of one strip segment
+// each from all over the matrix (131072 x 5120 with one group: 456 -> 432 us).
+// Shorter groups keep one band (there the strips already line up: 16640 x
+// 5120 with one group measured 60.4 us as one band, 61.7 us cut into bands).
+// Every role walks its run in order, so it keeps a cursor (group, band, K
+// tile, M tile) that advances one tile at a time: one search of the group
+// table per run instead of a search and a division per tile (the search alone
+// cost about 2 us per doubling of the group count at 16640 x 5120).
+constexpr int64_t kBandMinRun = 64;   // runs shorter than this: no bands
+
 struct GroupCursor {
   int g;
   int64_t tr_g, n_tg, tk, tm, start, end;
+  int64_t run;      // tiles per run (the band height of tall groups)
+  int64_t bh;       // this group's band height: run, or n_tg (one band)
+  int64_t b0, nb;   // first tile-row and tile-rows of the current band
 
   __device__ __forceinline__ void set_group(const GroupTab& tab, int gi) {
     g = gi;
@@ -248,8 +259,14 @@ struct GroupCursor {
     n_tg = tab.tr(gi + 1) - tr_g;
     start = gi ? tab.end(gi - 1) : 0;
     end = tab.end(gi);
+    bh = (run >= kBandMinRun && n_tg >= 2 * run) ? run : (n_tg > 0 ? n_tg : 1);
+    b0 = 0;
+    nb = n_tg < bh ? n_tg : bh;
+    tm = 0;
   }
-  __device__ __forceinline__ void init(const Params& p, const GroupTab& tab, int64_t t) {
+  __device__ __forceinline__ void init(const Params& p, const GroupTab& tab, int64_t t,
+                                       int64_t run_len) {
+    run = run_len;
     int lo = 0, hi = p.G;                          // tr(lo)*n_kt <= t < tr(hi)*n_kt
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -257,14 +274,28 @@ struct GroupCursor {
     }
     set_group(tab, lo);
     tk = 0;
-    tm = 0;
-    if (n_tg > 0) tk = div_tiles(t - tr_g * p.n_kt, n_tg, tm);   // else: past the last tile
+    if (n_tg > 0) {                                // else: past the last tile
+      const int64_t tl = t - tr_g * p.n_kt;
+      int64_t in_band;
+      const int64_t band = div_tiles(tl, bh * p.n_kt, in_band);
+      b0 = band * bh;
+      nb = n_tg - b0 < bh ? n_tg - b0 : bh;
+      int64_t r;
+      tk = div_tiles(in_band, nb, r);
+      tm = b0 + r;
+    }
   }
   __device__ __forceinline__ void next(const Params& p, const GroupTab& tab) {
-    if (++tm < n_tg) return;
-    tm = 0;
+    if (++tm < b0 + nb) return;
+    tm = b0;
     if (++tk < p.n_kt) return;
     tk = 0;
+    b0 += nb;
+    if (b0 < n_tg) {                               // next band of the group
+      nb = n_tg - b0 < bh ? n_tg - b0 : bh;
+      tm = b0;
+      return;
+    }
     int ng = g + 1;
     while (ng < p.G && tab.tr(ng + 1) == tab.tr(ng)) ++ng;   // skip empty groups
     if (ng < p.G) set_group(tab, ng);
@@ -276,7 +307,7 @@ struct GroupCursor {
     T.m0 = static_cast<int32_t>(m0);
     T.k0 = static_cast<int32_t>(tk * kTile);
     T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
-    T.cont = (tm > 0 ? 1 : 0) | (tm + 1 < n_tg ? 2 : 0);
+    T.cont = (tm > b0 ? 1 : 0) | (tm + 1 < b0 + nb ? 2 : 0);
     T.s0_dst = p.s0 + ((tr_g + tm) * p.n_kt + tk) * kScaleTile;
     T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (tr_g * 4) + (tk * n_tg + tm) * kScaleTile;
     return T;
@@ -297,14 +328,6 @@ __device__ __forceinline__ Tile role_tile(const Params& p, const GroupTab& tab, 
 }
 
 // ---- compute units ----------------------------------------------------------
-
-// Sixteen e4m3 NaN bytes (0x7F), the elements of a block whose scale is the
-// e8m0 NaN (0xFF): the product with a NaN multiplier converts to an e4m3 NaN
-// already, but with whichever sign the NaN carries, so the bytes are set
-// outright.
-__device__ __forceinline__ uint4 nan_e4m3x16() {
-  return make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-}
 
 // dim0 half-block unit (16 elements), stored straight to q0.  In warp step
 // with first row R0 (even), lane l takes row R0 + ((l >> 2) & 1) + 2*(l >> 4),
@@ -342,7 +365,6 @@ __device__ __forceinline__ void dim0_half_unit(const uint8_t* in, uint8_t* sc0, 
   o.y = e4m3x4(bf_lo(v0.z), bf_hi(v0.z), bf_lo(v0.w), bf_hi(v0.w), m);
   o.z = e4m3x4(bf_lo(v1.x), bf_hi(v1.x), bf_lo(v1.y), bf_hi(v1.y), m);
   o.w = e4m3x4(bf_lo(v1.z), bf_hi(v1.z), bf_lo(v1.w), bf_hi(v1.w), m);
-  if (sbyte == 0xFFu) o = nan_e4m3x16();          // Inf / NaN block: every element NaN
   const int64_t gr = static_cast<int64_t>(m0) + row;
   const int64_t gc = static_cast<int64_t>(k0) + 64 * box + 16 * hq;
   if (row < rows && gr < M && gc < K && in_span(p.sp_q0, q0 + gr * K + gc, 16))
@@ -410,8 +432,6 @@ __device__ __forceinline__ uint32_t dim1_unit(const uint8_t* in, uint8_t* q1s, u
   o0.z = MX_COL4_HI(w, 8, mo);  o0.w = MX_COL4_HI(w, 12, mo);
   o1.x = MX_COL4_HI(w, 16, mo); o1.y = MX_COL4_HI(w, 20, mo);
   o1.z = MX_COL4_HI(w, 24, mo); o1.w = MX_COL4_HI(w, 28, mo);
-  if (se == 0xFFu) e0 = e1 = nan_e4m3x16();       // Inf / NaN block: every element NaN
-  if (so == 0xFFu) o0 = o1 = nan_e4m3x16();
   const int sw = p & 7;
   uint8_t* de = q1s + p * 128;
   uint8_t* dodd = q1s + kQ1Half + p * 128;
@@ -610,6 +630,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
 
   GroupTab tab = {nullptr, nullptr, p.row_offs, p.offs};
   int64_t first, end, step;
+  int64_t run_len = 1;                        // grouped: tiles per CTA run (rounded up)
   if (kMode == kModeGrouped) {
     int64_t total_tr;                         // padded tile-rows of all groups
     if (p.G <= kMaxSmemGroups) {
@@ -679,6 +700,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     first = n_tiles * blockIdx.x / gridDim.x;
     end = n_tiles * (blockIdx.x + 1) / gridDim.x;
     step = 1;
+    run_len = (n_tiles + gridDim.x - 1) / gridDim.x;
   } else {
     first = blockIdx.x;
     end = p.n_tiles;
@@ -707,10 +729,18 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       prefetch_tmap(&tm_x);
       typename ItType<kMode>::T it = 0;
       GroupCursor cur;
-      if (kMode == kModeGrouped) cur.init(p, tab, first);
+      if (kMode == kModeGrouped) cur.init(p, tab, first, run_len);
       for (int64_t t = first; t < end; t += step, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+        if (static_cast<int64_t>(it) == p.stall_at && blockIdx.x == 0) {
+          // Diagnostic (armed from the host only): instead of loading this
+          // tile, wait on a barrier that nothing completes.  The wait runs
+          // out and raises the abort flag; the compute warps, waiting for
+          // this tile, and the store warp stop on it.
+          mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);
+          break;
+        }
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
         const Tile T = role_tile<kMode>(p, tab, t, cur);
         uint8_t* dst = smem + kOffIn + s * kInBytes;
@@ -729,7 +759,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     }
     typename ItType<kMode>::T it = 0;
     GroupCursor cur;
-    if (kMode == kModeGrouped) cur.init(p, tab, first);
+    if (kMode == kModeGrouped) cur.init(p, tab, first, run_len);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
@@ -803,17 +833,12 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     // compute warps
     typename ItType<kMode>::T it = 0;
     GroupCursor cur;
-    if (kMode == kModeGrouped) cur.init(p, tab, first);
+    if (kMode == kModeGrouped) cur.init(p, tab, first, run_len);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
       const int o = static_cast<int>(it % kStaging);
       const uint32_t oph = static_cast<uint32_t>((it / kStaging) & 1);
-      if (static_cast<int64_t>(it) == p.stall_at && blockIdx.x == 0) {
-        // Diagnostic (armed from the host only): a wait that runs out.
-        mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);
-        break;
-      }
       bool ok = mbar_wait(&full[s], ph, abort_flag);
       ok = ok && mbar_wait(&sempty[o], oph ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;

@@ -10,8 +10,11 @@
 //   mult  = 2^(127 - s)            exact float built from bits
 //   q_i   = e4m3 of x_i * mult, round to nearest even, saturate to +-448
 // The exponent comes from integer bit fields (no float log, as the review of
-// that PR asks).  E == 255 (Inf or NaN in the block) gives s = 0xFF and NaN
-// elements.
+// that PR asks).  E == 255 (Inf or NaN in the block) gives s = 0xFF and a
+// NaN multiplier; the product of any element with it is the positive
+// canonical NaN, which the e4m3 conversion writes as 0x7F, so every element
+// of such a block is 0x7F whatever the sign or payload of its NaN (the GPU
+// tests check these bytes).
 #pragma once
 
 #include <cuda.h>

@@ -227,6 +227,12 @@ __global__ void __launch_bounds__(kDqTmaThreads, 1)
       int64_t it = 0;
       for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
         const int s = static_cast<int>(it % kDqStages);
+        if (it == p.stall_at && blockIdx.x == 0) {
+          // Diagnostic (armed from the host only): a wait that runs out in
+          // place of this tile's loads; every role stops on the abort flag.
+          mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);
+          break;
+        }
         if (!mbar_wait(&empty[s], static_cast<uint32_t>(((it / kDqStages) & 1) ^ 1), abort_flag))
           break;
         const int64_t tr = t / p.n_tc, tc = t - tr * p.n_tc;
@@ -277,11 +283,6 @@ __global__ void __launch_bounds__(kDqTmaThreads, 1)
     for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
       const int s = static_cast<int>(it % kDqStages);
       const int o = static_cast<int>(it % kDqStaging);
-      if (it == p.stall_at && blockIdx.x == 0) {
-        // Diagnostic (armed from the host only): a wait that runs out.
-        mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);
-        break;
-      }
       bool ok = mbar_wait(&full[s], static_cast<uint32_t>((it / kDqStages) & 1), abort_flag);
       ok = ok && mbar_wait(&sempty[o], static_cast<uint32_t>(((it / kDqStaging) & 1) ^ 1),
                            abort_flag);

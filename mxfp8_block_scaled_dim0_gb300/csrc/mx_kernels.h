@@ -46,10 +46,11 @@ struct CastMaps {
 };
 
 // Diagnostic stall, armed from the host (mx_selftest_arm_stall) for the next
-// cast or bulk-staged rowwise launch of the arming thread: CTA 0's compute
-// threads wait, at their `at`-th tile (or step), on a barrier that nothing
-// completes, for at most `ns` nanoseconds, so that the wait runs out and the
-// CTA winds down through its abort path.  at < 0: none (normal use).
+// cast, tiled dequantisation or bulk-staged rowwise launch of the arming
+// thread: in CTA 0, the thread that issues the loads waits, at its `at`-th
+// tile (or step), on a barrier that nothing completes, for at most `ns`
+// nanoseconds, so that the wait runs out and the CTA winds down through its
+// abort path.  at < 0: none (normal use).
 struct Stall {
   int64_t at;
   uint64_t ns;
@@ -87,7 +88,7 @@ struct DqMaps {
   CUtensorMap q;
   CUtensorMap out;
 };
-constexpr int64_t kDqTmaMinCols = 128;
+constexpr int64_t kDqTmaMinCols = 1024;
 int launch_dequant_blocked(const DqMaps* maps, const uint8_t* q, int64_t R, int64_t C,
                            const uint8_t* s_blk, uint16_t* out, int num_sms, cudaStream_t stream);
 int read_dequant_watchdog(int* out, bool clear);

@@ -308,20 +308,24 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
     fence_mbar_init();
   }
   __syncthreads();
+  // Diagnostic stall (armed from the host only): in CTA 0, thread 0 waits,
+  // in place of issuing step stall_at's copy, on a barrier that nothing
+  // completes; the wait runs out and raises the abort flag, and every thread
+  // waiting for that step stops on it.
+  const int64_t stall_i = blockIdx.x == 0 ? stall_at : -1;
   int64_t issued = 0;                        // meaningful in thread 0
   if (threadIdx.x == 0)
-    for (; issued < stages && issued < n_steps; ++issued) issue(issued);
+    for (; issued < stages && issued < n_steps; ++issued) {
+      if (issued == stall_i) {
+        mbar_wait(&stall_bar, 0u, &abort_flag, stall_ns);
+        break;
+      }
+      issue(issued);
+    }
 
   int64_t i = 0;
   for (; i < n_steps; ++i) {
     const int st = static_cast<int>(i % stages);
-    if (i == stall_at && blockIdx.x == 0) {
-      // Diagnostic (armed from the host only): a wait that runs out; every
-      // thread of the CTA takes it, and the abort path below lets the copies
-      // in flight land.
-      mbar_wait(&stall_bar, 0u, &abort_flag, stall_ns);
-      break;
-    }
     const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((i / stages) & 1), &abort_flag);
     if (!__syncthreads_and(ok)) break;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * groups + i * step_rows + g;
@@ -355,7 +359,12 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
       }
     }
     __syncthreads();                          // every thread is done with this stage
-    if (threadIdx.x == 0 && i + stages < n_steps) issue(issued++);
+    if (threadIdx.x == 0 && i + stages < n_steps) {
+      if (issued == stall_i)
+        mbar_wait(&stall_bar, 0u, &abort_flag, stall_ns);
+      else
+        issue(issued++);
+    }
   }
   if (threadIdx.x == 0 && abort_flag) {
     // Gave up waiting: let the copies still in flight land (bounded) before

@@ -196,11 +196,11 @@ def test_dequant_every_element_every_scale():
 
 
 def test_dequant_every_element_every_scale_tiled():
-    """The same 65,536 (element, scale) pairs laid out in rows of 128 values,
-    the tiled kernel's path: block b (row b // 4, scale column b % 4) has scale
-    byte b % 256 and elements (32 (b // 256) + i) % 256, so every scale byte
-    meets every element byte four times."""
-    R, C = 2048, 128
+    """The same 65,536 (element, scale) pairs laid out in rows of 1024 values,
+    the tiled kernel's path: block b (row b // 32, scale column b % 32) has
+    scale byte b % 256 and elements (32 (b // 256) + i) % 256, so every scale
+    byte meets every element byte four times."""
+    R, C = 256, 1024
     b = np.arange(R * C // 32)
     s = (b % 256).astype(np.uint8).reshape(R, C // 32)
     q = ((32 * (b[:, None] // 256) + np.arange(32)[None, :]) % 256).astype(np.uint8)
@@ -224,11 +224,11 @@ def test_dequant_of_cast_matches_oracle(M, K):
     assert_bf16_equal(bf16_np(d1), oracle.dequant_blocked(oq1, os1), "dequant dim1")
 
 
-# Rows shorter than 128 values take the thread-store kernel, longer ones the
+# Rows shorter than 1024 values take the thread-store kernel, longer ones the
 # tiled kernel, whose last tile column may hold only 32 .. 96 columns (C % 128
 # != 0) and whose last tile row may be partial.
-@pytest.mark.parametrize("R,C", [(1, 32), (77, 96), (3, 8192), (1, 128), (77, 160), (129, 4128),
-                                 (300, 224), (130, 1056)])
+@pytest.mark.parametrize("R,C", [(1, 32), (77, 96), (1, 128), (77, 160), (300, 224), (3, 8192),
+                                 (1, 1024), (129, 4128), (130, 1056), (77, 1120), (5, 1056)])
 def test_dequant_ragged_shapes(R, C):
     rng = np.random.default_rng(R * 7 + C)
     q = rng.integers(0, 256, size=(R, C), dtype=np.uint8)

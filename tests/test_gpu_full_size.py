@@ -6,6 +6,8 @@
   experts16x8192x5120  (16, 8192, 5120) bf16 expert weights: the per-expert
                        dim1 cast (mx_cast_3d_dim1), and the dim0 and fused
                        dim0 + dim1 casts of the same weights
+  grouped, tall group  (65536, 5120) MoE activations in 3 groups, one of them
+                       tall enough for the grouped kernel's banded tile order
 
 The inputs are generated on the GPU (the same recipe as on the CPU, drawn by
 the CUDA generator), copied to the host once, and cast by the oracle spread
@@ -107,3 +109,19 @@ def test_experts_dim0_and_fused_every_byte(experts_case):
     assert_bytes_equal(to_np(s0), os0, "fused s0 per expert")
     assert_bytes_equal(to_np(q1), oq1, "fused q1")
     assert_bytes_equal(to_np(s1), os1, "fused s1 per expert")
+
+
+def test_grouped_tall_group_every_byte():
+    """Grouped-M cast with a group far taller than a CTA's run of tiles
+    (65536 x 5120; groups of 40000, 1 and 25535 rows): the tall group's tiles
+    are walked in bands of tile-rows, the others as whole column strips; every
+    output byte against the oracle."""
+    M, K = 65536, 5120
+    x = W.normal((M, K), 1006, device="cuda")
+    offs = [40000, 40001, 65536]
+    got = mx.cast_grouped_m(x, torch.tensor(offs, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(got[6].item()) == 0
+    want = oracle.cast_grouped_m(W.bf16_bits(x), np.array(offs, np.int32))
+    for name, g, w in zip(("q0", "s0", "s0_row_offs", "q1", "s1", "s1_col_offs"), got, want):
+        assert_bytes_equal(to_np(g), w, name)
