@@ -256,8 +256,9 @@ int mx_selftest_bounds(void* buf16, void* stream);
  * any fault.  Returns MX_OK, MX_ERR_SHAPE or MX_ERR_CUDA. */
 int mx_selftest_watchdog(int64_t wait_ns, void* stream);
 
-/* Diagnostic: arm a stall for the calling thread's next launch of a kernel
- * whose waits are bounded (the cast kernels of mx_cast_dim0_dim1,
+/* Diagnostic of checked builds (compiled with -DMX_DEBUG_BOUNDS, as
+ * libmxfp8_cast_bounds.so): arm a stall for the calling thread's next launch
+ * of a kernel whose waits are bounded (the cast kernels of mx_cast_dim0_dim1,
  * mx_cast_dim0, mx_cast_dim1, mx_cast_grouped_m and the 3D casts; the
  * bulk-staged kernel of mx_cast_rowwise, used for K <= 24576; the tiled
  * kernel of mx_dequant_blocked, used for C >= 1024).  In that launch the
@@ -267,8 +268,9 @@ int mx_selftest_watchdog(int64_t wait_ns, void* stream);
  * copies it has in flight land, sets the word read by mx_watchdog(), and the
  * kernel returns normally: the abort path of a real cast, exercised without
  * any fault.  That launch's outputs are incomplete.  Without a kernel to take
- * it the stall stays armed; a launch consumes it.  Returns MX_OK or
- * MX_ERR_SHAPE (at < 0 or wait_ns out of range). */
+ * it the stall stays armed; a launch consumes it.  Returns MX_OK,
+ * MX_ERR_SHAPE (at < 0 or wait_ns out of range), or -1 in a release build,
+ * whose kernels carry no stall hook (nothing is armed). */
 int mx_selftest_arm_stall(int64_t at, int64_t wait_ns);
 
 #ifdef __cplusplus

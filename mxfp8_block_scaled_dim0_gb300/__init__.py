@@ -335,10 +335,14 @@ def mx_selftest_watchdog(wait_ns=50_000_000, stream=None):
 
 
 def mx_selftest_arm_stall(at, wait_ns=20_000_000):
-    """Arm a stall for this thread's next cast (or bulk-staged rowwise)
-    launch: CTA 0 gives up waiting at its `at`-th tile and takes the abort
-    path, without any fault (see include/mxfp8_cast.h)."""
-    _check(_lib().mx_selftest_arm_stall(int(at), int(wait_ns)), "mx_selftest_arm_stall")
+    """Checked builds: arm a stall for this thread's next cast, tiled
+    dequantisation or bulk-staged rowwise launch.  CTA 0 gives up waiting at
+    its `at`-th tile and takes the abort path, without any fault (see
+    include/mxfp8_cast.h).  A release build has no stall hook."""
+    rc = _lib().mx_selftest_arm_stall(int(at), int(wait_ns))
+    if rc == -1:
+        raise RuntimeError("mx_selftest_arm_stall: release build, no stall hook compiled in")
+    _check(rc, "mx_selftest_arm_stall")
 
 
 def mx_bounds_check(clear=True):

@@ -251,7 +251,7 @@ struct GroupCursor {
   int64_t tr_g, n_tg, tk, tm, start, end;
   int64_t run;      // tiles per run (the band height of tall groups)
   int64_t bh;       // this group's band height: run, or n_tg (one band)
-  int64_t b0, nb;   // first tile-row and tile-rows of the current band
+  int64_t b0, bend; // first tile-row and end tile-row of the current band
 
   __device__ __forceinline__ void set_group(const GroupTab& tab, int gi) {
     g = gi;
@@ -261,7 +261,7 @@ struct GroupCursor {
     end = tab.end(gi);
     bh = (run >= kBandMinRun && n_tg >= 2 * run) ? run : (n_tg > 0 ? n_tg : 1);
     b0 = 0;
-    nb = n_tg < bh ? n_tg : bh;
+    bend = n_tg < bh ? n_tg : bh;
     tm = 0;
   }
   __device__ __forceinline__ void init(const Params& p, const GroupTab& tab, int64_t t,
@@ -279,20 +279,20 @@ struct GroupCursor {
       int64_t in_band;
       const int64_t band = div_tiles(tl, bh * p.n_kt, in_band);
       b0 = band * bh;
-      nb = n_tg - b0 < bh ? n_tg - b0 : bh;
+      bend = n_tg - b0 < bh ? n_tg : b0 + bh;
       int64_t r;
-      tk = div_tiles(in_band, nb, r);
+      tk = div_tiles(in_band, bend - b0, r);
       tm = b0 + r;
     }
   }
   __device__ __forceinline__ void next(const Params& p, const GroupTab& tab) {
-    if (++tm < b0 + nb) return;
+    if (++tm < bend) return;
     tm = b0;
     if (++tk < p.n_kt) return;
     tk = 0;
-    b0 += nb;
+    b0 = bend;
     if (b0 < n_tg) {                               // next band of the group
-      nb = n_tg - b0 < bh ? n_tg - b0 : bh;
+      bend = n_tg - b0 < bh ? n_tg : b0 + bh;
       tm = b0;
       return;
     }
@@ -307,7 +307,7 @@ struct GroupCursor {
     T.m0 = static_cast<int32_t>(m0);
     T.k0 = static_cast<int32_t>(tk * kTile);
     T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
-    T.cont = (tm > b0 ? 1 : 0) | (tm + 1 < b0 + nb ? 2 : 0);
+    T.cont = (tm > b0 ? 1 : 0) | (tm + 1 < bend ? 2 : 0);
     T.s0_dst = p.s0 + ((tr_g + tm) * p.n_kt + tk) * kScaleTile;
     T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (tr_g * 4) + (tk * n_tg + tm) * kScaleTile;
     return T;
@@ -733,8 +733,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       for (int64_t t = first; t < end; t += step, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
-        if (static_cast<int64_t>(it) == p.stall_at && blockIdx.x == 0) {
-          // Diagnostic (armed from the host only): instead of loading this
+        if (kDiagStall && static_cast<int64_t>(it) == p.stall_at && blockIdx.x == 0) {
+          // Diagnostic (checked builds, armed from the host): instead of loading this
           // tile, wait on a barrier that nothing completes.  The wait runs
           // out and raises the abort flag; the compute warps, waiting for
           // this tile, and the store warp stop on it.

@@ -253,6 +253,16 @@ struct Span {
 static __device__ unsigned int g_out_of_bounds = 0;
 #endif
 
+// Checked builds also carry the diagnostic stall hook (mx_selftest_arm_stall:
+// a wait that runs out on purpose, to drive a kernel's abort path).  Release
+// builds compile it away: even a never-taken check where loads are issued
+// measured 0.2-0.7% on the cast kernels and 4% on the rowwise kernel.
+#ifdef MX_DEBUG_BOUNDS
+constexpr bool kDiagStall = true;
+#else
+constexpr bool kDiagStall = false;
+#endif
+
 __device__ __forceinline__ bool in_span(const Span& s, const void* p, uint64_t n) {
 #ifdef MX_DEBUG_BOUNDS
   const uint64_t a = reinterpret_cast<uint64_t>(p);

@@ -227,8 +227,8 @@ __global__ void __launch_bounds__(kDqTmaThreads, 1)
       int64_t it = 0;
       for (int64_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
         const int s = static_cast<int>(it % kDqStages);
-        if (it == p.stall_at && blockIdx.x == 0) {
-          // Diagnostic (armed from the host only): a wait that runs out in
+        if (kDiagStall && it == p.stall_at && blockIdx.x == 0) {
+          // Diagnostic (checked builds, armed from the host): a wait that runs out in
           // place of this tile's loads; every role stops on the abort flag.
           mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);
           break;

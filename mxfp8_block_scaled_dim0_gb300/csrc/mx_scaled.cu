@@ -308,15 +308,15 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
     fence_mbar_init();
   }
   __syncthreads();
-  // Diagnostic stall (armed from the host only): in CTA 0, thread 0 waits,
-  // in place of issuing step stall_at's copy, on a barrier that nothing
-  // completes; the wait runs out and raises the abort flag, and every thread
-  // waiting for that step stops on it.
-  const int64_t stall_i = blockIdx.x == 0 ? stall_at : -1;
+  // Diagnostic stall (checked builds, armed from the host): in CTA 0, thread
+  // 0 waits, in place of issuing step stall_at's copy, on a barrier that
+  // nothing completes; the wait runs out and raises the abort flag, and every
+  // thread waiting for that step stops on it.
+  const int64_t stall_i = kDiagStall && blockIdx.x == 0 ? stall_at : -1;
   int64_t issued = 0;                        // meaningful in thread 0
   if (threadIdx.x == 0)
     for (; issued < stages && issued < n_steps; ++issued) {
-      if (issued == stall_i) {
+      if (kDiagStall && issued == stall_i) {
         mbar_wait(&stall_bar, 0u, &abort_flag, stall_ns);
         break;
       }
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
     }
     __syncthreads();                          // every thread is done with this stage
     if (threadIdx.x == 0 && i + stages < n_steps) {
-      if (issued == stall_i)
+      if (kDiagStall && issued == stall_i)
         mbar_wait(&stall_bar, 0u, &abort_flag, stall_ns);
       else
         issue(issued++);

@@ -181,6 +181,17 @@ def test_bounds_entry_points_in_release_build(lib):
     assert lib.mx_selftest_bounds(A, None) == -1
 
 
+def test_stall_hook_only_in_the_checked_build(lib):
+    """Arming the diagnostic stall is host-only.  The release build has no
+    stall hook and says so (-1); the checked build arms it."""
+    assert lib.mx_selftest_arm_stall(0, 1_000_000) == -1
+    assert lib.mx_selftest_arm_stall(-1, 1_000_000) == mx.MX_ERR_SHAPE
+    blib = ctypes.CDLL(mxbuild.build(bounds=True))
+    blib.mx_selftest_arm_stall.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert blib.mx_selftest_arm_stall(0, 1_000_000) == mx.MX_OK
+    assert blib.mx_selftest_arm_stall(0, 10) == mx.MX_ERR_SHAPE
+
+
 def test_bounds_checked_library_exports_every_symbol():
     path = mxbuild.build(bounds=True)
     blib = ctypes.CDLL(path)
