@@ -386,7 +386,8 @@ def make_row(row, args, dev, rank):
             def build(i):
                 q, s_blk = mx.cast_dim0(gen(i))
                 return (q, s_blk, torch.empty((M, K), dtype=torch.bfloat16, device=dev))
-            return Row("dequant", wl, "dequant_blocked_kernel", M * K + blk(M, K // 32) + 2 * M * K,
+            kernel = "dequant_tma_kernel" if K >= 1024 else "dequant_blocked_kernel"
+            return Row("dequant", wl, kernel, M * K + blk(M, K // 32) + 2 * M * K,
                        1, build, lambda a, st: mx.mx_dequant_blocked(*a, stream=st), (0, 1), (2,))
 
         def build(i):

@@ -93,12 +93,16 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 //   kModeExperts0  the same for dim0
 //   kModeExperts01 the same for dim0 + dim1
 //   kModeGrouped   grouped-M activations: dim0 + dim1 per group
+//   kModeGroupedBands  the same, with tall groups walked in bands (see
+//                  GroupCursor); a separate instantiation, so that shapes
+//                  whose runs are too short for bands pay nothing for them
 enum Mode : int {
-  kModeFused2D = 0, kModeDim1 = 1, kModeExperts = 2, kModeGrouped = 3,
+  kModeFused2D = 0, kModeDim1 = 1, kModeExperts = 2, kModeGrouped = 3, kModeGroupedBands = 7,
   kModeDim0 = 4, kModeExperts0 = 5, kModeExperts01 = 6
 };
 __host__ __device__ constexpr bool has_dim0(int m) {
-  return m == kModeFused2D || m == kModeGrouped || m == kModeDim0 || m == kModeExperts0 ||
+  return m == kModeFused2D || m == kModeGrouped || m == kModeGroupedBands || m == kModeDim0 ||
+         m == kModeExperts0 ||
          m == kModeExperts01;
 }
 __host__ __device__ constexpr bool has_dim1(int m) { return m != kModeDim0 && m != kModeExperts0; }
@@ -110,7 +114,8 @@ __host__ __device__ constexpr bool per_expert(int m) {
 // the grouped mode q1 cannot leave by TMA (group starts are not 16-byte
 // aligned), so four store warps copy it out with plain stores, off the
 // compute warps' path.
-__host__ __device__ constexpr int store_warps(int mode) { return mode == kModeGrouped ? 4 : 1; }
+__host__ __device__ constexpr bool is_grouped(int m) { return m == kModeGrouped || m == kModeGroupedBands; }
+__host__ __device__ constexpr int store_warps(int mode) { return is_grouped(mode) ? 4 : 1; }
 __host__ __device__ constexpr int threads_of(int mode) {
   return (kComputeWarps + 1 + store_warps(mode)) * 32;
 }
@@ -198,6 +203,7 @@ __device__ __forceinline__ int64_t div_tiles(int64_t a, int64_t b, int64_t& r) {
 // 16640 x 5120, G = 4, measured against the 64-bit counter).
 template <int M> struct ItType { using T = int64_t; };
 template <> struct ItType<kModeGrouped> { using T = uint32_t; };
+template <> struct ItType<kModeGroupedBands> { using T = uint32_t; };
 
 // Tile t of the launch in the 2D / 3D modes: row-major over (M tiles, K tiles).
 template <int kMode>
@@ -246,12 +252,13 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, i
 // cost about 2 us per doubling of the group count at 16640 x 5120).
 constexpr int64_t kBandMinRun = 64;   // runs shorter than this: no bands
 
+template <bool kBands>
 struct GroupCursor {
   int g;
   int64_t tr_g, n_tg, tk, tm, start, end;
-  int64_t run;      // tiles per run (the band height of tall groups)
-  int64_t bh;       // this group's band height: run, or n_tg (one band)
-  int64_t b0, bend; // first tile-row and end tile-row of the current band
+  int64_t run;      // kBands: tiles per run (the band height of tall groups)
+  int64_t bh;       // kBands: this group's band height, run or n_tg (one band)
+  int64_t b0, bend; // kBands: first and end tile-row of the current band
 
   __device__ __forceinline__ void set_group(const GroupTab& tab, int gi) {
     g = gi;
@@ -259,10 +266,12 @@ struct GroupCursor {
     n_tg = tab.tr(gi + 1) - tr_g;
     start = gi ? tab.end(gi - 1) : 0;
     end = tab.end(gi);
-    bh = (run >= kBandMinRun && n_tg >= 2 * run) ? run : (n_tg > 0 ? n_tg : 1);
-    b0 = 0;
-    bend = n_tg < bh ? n_tg : bh;
     tm = 0;
+    if (kBands) {
+      bh = (run >= kBandMinRun && n_tg >= 2 * run) ? run : (n_tg > 0 ? n_tg : 1);
+      b0 = 0;
+      bend = n_tg < bh ? n_tg : bh;
+    }
   }
   __device__ __forceinline__ void init(const Params& p, const GroupTab& tab, int64_t t,
                                        int64_t run_len) {
@@ -274,8 +283,9 @@ struct GroupCursor {
     }
     set_group(tab, lo);
     tk = 0;
-    if (n_tg > 0) {                                // else: past the last tile
-      const int64_t tl = t - tr_g * p.n_kt;
+    if (n_tg <= 0) return;                         // past the last tile
+    const int64_t tl = t - tr_g * p.n_kt;
+    if (kBands) {
       int64_t in_band;
       const int64_t band = div_tiles(tl, bh * p.n_kt, in_band);
       b0 = band * bh;
@@ -283,18 +293,22 @@ struct GroupCursor {
       int64_t r;
       tk = div_tiles(in_band, bend - b0, r);
       tm = b0 + r;
+    } else {
+      tk = div_tiles(tl, n_tg, tm);
     }
   }
   __device__ __forceinline__ void next(const Params& p, const GroupTab& tab) {
-    if (++tm < bend) return;
-    tm = b0;
+    if (++tm < (kBands ? bend : n_tg)) return;
+    tm = kBands ? b0 : 0;
     if (++tk < p.n_kt) return;
     tk = 0;
-    b0 = bend;
-    if (b0 < n_tg) {                               // next band of the group
-      bend = n_tg - b0 < bh ? n_tg : b0 + bh;
-      tm = b0;
-      return;
+    if (kBands) {
+      b0 = bend;
+      if (b0 < n_tg) {                             // next band of the group
+        bend = n_tg - b0 < bh ? n_tg : b0 + bh;
+        tm = b0;
+        return;
+      }
     }
     int ng = g + 1;
     while (ng < p.G && tab.tr(ng + 1) == tab.tr(ng)) ++ng;   // skip empty groups
@@ -307,7 +321,8 @@ struct GroupCursor {
     T.m0 = static_cast<int32_t>(m0);
     T.k0 = static_cast<int32_t>(tk * kTile);
     T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
-    T.cont = (tm > b0 ? 1 : 0) | (tm + 1 < bend ? 2 : 0);
+    T.cont = kBands ? ((tm > b0 ? 1 : 0) | (tm + 1 < bend ? 2 : 0))
+                    : ((tm > 0 ? 1 : 0) | (tm + 1 < n_tg ? 2 : 0));
     T.s0_dst = p.s0 + ((tr_g + tm) * p.n_kt + tk) * kScaleTile;
     T.s1_dst = p.s1 + static_cast<int64_t>(p.k128) * (tr_g * 4) + (tk * n_tg + tm) * kScaleTile;
     return T;
@@ -316,10 +331,10 @@ struct GroupCursor {
 
 // The tile a role processes at run position t: from the cursor (advanced
 // past it) in the grouped mode, from t otherwise.
-template <int kMode>
+template <int kMode, typename Cursor>
 __device__ __forceinline__ Tile role_tile(const Params& p, const GroupTab& tab, int64_t t,
-                                          GroupCursor& cur) {
-  if (kMode == kModeGrouped) {
+                                          Cursor& cur) {
+  if (is_grouped(kMode)) {
     const Tile T = cur.tile(p);
     cur.next(p, tab);
     return T;
@@ -606,7 +621,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
                    const __grid_constant__ CUtensorMap tm_q1o, const Params p) {
   constexpr bool kDim0 = has_dim0(kMode);
   constexpr bool kDim1 = has_dim1(kMode);
-  constexpr bool kTmaQ1 = kDim1 && kMode != kModeGrouped;
+  constexpr bool kTmaQ1 = kDim1 && !is_grouped(kMode);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -631,7 +646,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   GroupTab tab = {nullptr, nullptr, p.row_offs, p.offs};
   int64_t first, end, step;
   int64_t run_len = 1;                        // grouped: tiles per CTA run (rounded up)
-  if (kMode == kModeGrouped) {
+  if (is_grouped(kMode)) {
     int64_t total_tr;                         // padded tile-rows of all groups
     if (p.G <= kMaxSmemGroups) {
       // Up to kMaxSmemGroups groups every CTA builds the group table itself
@@ -728,8 +743,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     if (lane == 0) {
       prefetch_tmap(&tm_x);
       typename ItType<kMode>::T it = 0;
-      GroupCursor cur;
-      if (kMode == kModeGrouped) cur.init(p, tab, first, run_len);
+      GroupCursor<kMode == kModeGroupedBands> cur;
+      if (is_grouped(kMode)) cur.init(p, tab, first, run_len);
       for (int64_t t = first; t < end; t += step, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
@@ -758,8 +773,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       prefetch_tmap(&tm_q1o);
     }
     typename ItType<kMode>::T it = 0;
-    GroupCursor cur;
-    if (kMode == kModeGrouped) cur.init(p, tab, first, run_len);
+    GroupCursor<kMode == kModeGroupedBands> cur;
+    if (is_grouped(kMode)) cur.init(p, tab, first, run_len);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
@@ -767,7 +782,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       const Tile T = role_tile<kMode>(p, tab, t, cur);
       uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
-      if (kMode == kModeGrouped) {
+      if (is_grouped(kMode)) {
         // Grouped: store warp sw owns rows 16*sw .. 16*sw+15 of each q1 half.
         // A whole 128-row tile whose q1 rows are 16-byte aligned at a common
         // offset leaves by TMA (one 16-row box per half and warp), shifted
@@ -832,8 +847,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   } else {
     // compute warps
     typename ItType<kMode>::T it = 0;
-    GroupCursor cur;
-    if (kMode == kModeGrouped) cur.init(p, tab, first, run_len);
+    GroupCursor<kMode == kModeGroupedBands> cur;
+    if (is_grouped(kMode)) cur.init(p, tab, first, run_len);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
@@ -866,7 +881,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       uint32_t sb = 0;
       if (!kDim1)
         ;
-      else if (kMode == kModeGrouped && T.rows < kTile)
+      else if (is_grouped(kMode) && T.rows < kTile)
         sb = dim1_unit<true>(in, q1s, sc1, pcol, mb, T.rows);
       else
         sb = dim1_unit<false>(in, q1s, sc1, pcol, mb, T.rows);
@@ -896,7 +911,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       if (lane == 0) mbar_arrive(&sfull[o]);
     }
 
-    if (kMode == kModeGrouped) {
+    if (is_grouped(kMode)) {
       // Zero the scale buffers' tails beyond the last group's padded end.
       const int64_t kb4 = static_cast<int64_t>(p.n_kt) * 4;
       const int64_t s0_beg = tab.tr(p.G) * 128 * kb4;
@@ -1072,7 +1087,10 @@ int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_
   }
   const int64_t bound = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
   const int grid = static_cast<int>(bound < num_sms ? (bound > 0 ? bound : 1) : num_sms);
-  return launch<kModeGrouped>(maps, prm, grid, stream);
+  // A CTA's run is at most ceil(bound / grid) tiles: below kBandMinRun no
+  // group can be banded, and the plain cursor is taken.
+  if ((bound + grid - 1) / grid < kBandMinRun) return launch<kModeGrouped>(maps, prm, grid, stream);
+  return launch<kModeGroupedBands>(maps, prm, grid, stream);
 }
 
 // Watchdog self-test: one warp waits on an mbarrier that nothing arrives at,

@@ -86,6 +86,26 @@ def test_grouped_in_bounds(M, K, offs):
     no_refused_stores()
 
 
+def test_grouped_banded_in_bounds():
+    """A shape whose CTA runs reach 64 tiles takes the banded grouped kernel:
+    40960 x 4096 with a 30000-row group (banded) and a 10960-row group (one
+    band)."""
+    import os
+    M, K = 40960, 4096
+    offs = [30000, 40960]
+    x = W.normal((M, K), 41, device="cuda")
+    got = mx.cast_grouped_m(x, torch.tensor(offs, dtype=torch.int32, device="cuda"))
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        want = oracle.cast_grouped_m(W.bf16_bits(x), np.array(offs, np.int32))
+    finally:
+        oracle.set_threads(1)
+    for i, name in enumerate(("q0", "s0", "r0", "q1", "s1", "c1")):
+        eq(got[i], want[i], name)
+    assert int(got[6].item()) == 0
+    no_refused_stores()
+
+
 @pytest.mark.parametrize("E,N,K", [(2, 96, 160), (3, 256, 160), (3, 50, 96)])
 def test_3d_in_bounds(E, N, K):
     w = W.experts(E, N, K, E * N + K)
