@@ -7,7 +7,9 @@
                        dim1 cast (mx_cast_3d_dim1), and the dim0 and fused
                        dim0 + dim1 casts of the same weights
   grouped, tall group  (65536, 5120) MoE activations in 3 groups, one of them
-                       tall enough for the grouped kernel's banded tile order
+                       tall enough for the grouped kernel's banded tile order;
+                       and (400000, 512) in 1101 groups (banded order with the
+                       group table in global memory)
 
 The inputs are generated on the GPU (the same recipe as on the CPU, drawn by
 the CUDA generator), copied to the host once, and cast by the oracle spread
@@ -123,5 +125,25 @@ def test_grouped_tall_group_every_byte():
     torch.cuda.synchronize()
     assert int(got[6].item()) == 0
     want = oracle.cast_grouped_m(W.bf16_bits(x), np.array(offs, np.int32))
+    for name, g, w in zip(("q0", "s0", "s0_row_offs", "q1", "s1", "s1_col_offs"), got, want):
+        assert_bytes_equal(to_np(g), w, name)
+
+
+def test_grouped_banded_with_many_groups_every_byte():
+    """More than 1024 groups take the separate offsets kernel and a group
+    table in global memory.  400000 x 512 in 1101 groups (300000 rows, 1099
+    groups of 45 rows, then 50545 rows) makes the runs 101 tiles long, so the
+    two tall groups are walked in bands: both paths together, every byte
+    against the oracle."""
+    M, K = 400000, 512
+    sizes = [300000] + [45] * 1099
+    sizes.append(M - sum(sizes))
+    offs = np.cumsum(sizes).astype(np.int32)
+    assert len(offs) == 1101 and offs[-1] == M and sizes[-1] == 50545
+    x = W.normal((M, K), 1007, device="cuda")
+    got = mx.cast_grouped_m(x, torch.from_numpy(offs).cuda())
+    torch.cuda.synchronize()
+    assert int(got[6].item()) == 0
+    want = oracle.cast_grouped_m(W.bf16_bits(x), offs)
     for name, g, w in zip(("q0", "s0", "s0_row_offs", "q1", "s1", "s1_col_offs"), got, want):
         assert_bytes_equal(to_np(g), w, name)
