@@ -228,9 +228,11 @@ const char* mx_strerror(int code);
 /* cudaError_t value of the last failed CUDA call made by this thread. */
 int mx_last_cuda_error(void);
 
-/* Device watchdog: every wait inside the kernels is bounded; a CTA that gives
- * up sets a device word.  Returns that word (0 or 1) after synchronising the
- * current device, clearing it if `clear` is non-zero, or MX_ERR_CUDA. */
+/* Device watchdog: every wait inside the kernels is bounded.  A CTA that
+ * gives up stops all its roles, lets the copies it has in flight land, and
+ * sets a device word (one per kernel file).  Returns the words OR-ed (0 or 1)
+ * after synchronising the current device, clearing them if `clear` is
+ * non-zero, or MX_ERR_CUDA. */
 int mx_watchdog(int clear);
 
 /* Bounds-checked builds (compiled with -DMX_DEBUG_BOUNDS): the number of
