@@ -133,6 +133,14 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x,
                : "memory");
 }
 
+// Hint: bring `bytes` bytes at g into L2 (g 16-byte aligned, bytes a
+// multiple of 16).  No data reaches the SM and nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* g, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(g)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t x, int32_t y,
                                              const void* smem_src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::

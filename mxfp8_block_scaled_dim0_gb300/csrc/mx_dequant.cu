@@ -102,6 +102,27 @@ __device__ __forceinline__ uint4 dequant8(uint2 v, float m) {
 
 __global__ void __launch_bounds__(kDqThreads) dequant_blocked_kernel(const DqParams p) {
   asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) {
+    // While earlier grids finish, ask L2 for this CTA's first tiles of q (a
+    // hint only; every access waits below): whole rows of a band, or 2 KB
+    // of one row.
+    for (int u = 0; u < kDqUnroll; ++u) {
+      const int64_t t = blockIdx.x + static_cast<int64_t>(u) * gridDim.x;
+      if (t >= p.n_tiles) break;
+      const int64_t band = t / p.n_ct, ct = t - band * p.n_ct;
+      int64_t off, bytes;
+      if (p.rpt > 1 || p.cpr < kDqThreads) {
+        const int64_t r0 = band * p.rpt;
+        off = r0 * p.C;
+        bytes = (p.R - r0 < p.rpt ? p.R - r0 : p.rpt) * p.C;
+      } else {
+        off = band * p.C + ct * (8 * kDqThreads);
+        bytes = p.C - ct * (8 * kDqThreads);
+        if (bytes > 8 * kDqThreads) bytes = 8 * kDqThreads;
+      }
+      bulk_prefetch_l2(p.q + off, static_cast<uint32_t>(bytes));
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // This thread's place inside a tile: row offset within the band and chunk.
@@ -215,8 +236,20 @@ __global__ void __launch_bounds__(kDqTmaThreads, 1)
     fence_mbar_init();
   }
   // Programmatic dependent launch: the barriers above touch no global memory;
-  // every global access waits for the earlier grids.
+  // every global access waits for the earlier grids.  Meanwhile the producer
+  // asks L2 for the tiles its ring loads first (a hint only: nothing reaches
+  // the SM before the wait, and the loads after it see the earlier grids'
+  // writes, L2 being where global memory is coherent).
   asm volatile("griddepcontrol.launch_dependents;");
+  if (warp == kDqProducerWarp && lane == 0) {
+    for (int i = 0; i < kDqStages; ++i) {
+      const int64_t t = blockIdx.x + static_cast<int64_t>(gridDim.x) * i;
+      if (t >= p.n_tiles) break;
+      const int64_t tr = t / p.n_tc, tc = t - tr * p.n_tc;
+      tma_prefetch_2d(&tm_q, static_cast<int32_t>(tc * kDqTile), static_cast<int32_t>(tr * kDqTile));
+      bulk_prefetch_l2(p.s + (tr * p.s_tiles_row + tc) * kDqScaleBytes, kDqScaleBytes);
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
 

@@ -272,7 +272,6 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
                                                                 Span sp_q, Span sp_scale,
                                                                 int64_t stall_at, uint64_t stall_ns) {
   asm volatile("griddepcontrol.launch_dependents;");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint32_t red[kThreads / 32];
   __shared__ __align__(8) uint64_t full[8];
@@ -287,6 +286,17 @@ __global__ void __launch_bounds__(kThreads) rowwise_bulk_kernel(const uint16_t* 
   const int64_t stage_bytes = row_bytes * groups;
   const int64_t step_rows = static_cast<int64_t>(gridDim.x) * groups;
   const int64_t n_steps = (M - static_cast<int64_t>(blockIdx.x) * groups + step_rows - 1) / step_rows;
+  if (threadIdx.x == 0) {
+    // While earlier grids finish, ask L2 for the rows of this CTA's first
+    // steps (a hint only: nothing reaches the SM before the wait, and the
+    // copies after it see the earlier grids' writes).
+    for (int64_t i = 0; i < stages && i < n_steps; ++i) {
+      const int64_t r0 = static_cast<int64_t>(blockIdx.x) * groups + i * step_rows;
+      const int64_t rows = M - r0 < groups ? M - r0 : groups;
+      bulk_prefetch_l2(x + r0 * K, static_cast<uint32_t>(rows * row_bytes));
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   auto issue = [&](int64_t i) {             // thread 0: step i into its stage
     const int st = static_cast<int>(i % stages);
