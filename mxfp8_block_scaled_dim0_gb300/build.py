@@ -2,7 +2,7 @@
 
 Each CUDA translation unit is compiled for sm_103a only, in parallel, then
 linked into one shared library next to this file.  The CUDA runtime is linked
-statically and the driver's tensor-map encoder is looked up at run time, so the
+statically and the CUDA driver's tensor-map encoder is looked up at run time, so the
 library loads on a machine without a GPU (for symbol checks).
 """
 import concurrent.futures as cf
