@@ -680,7 +680,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   // Programmatic dependent launch: let the next launch in the stream start
   // its set-up now (it cannot share an SM with this CTA, so it only takes SMs
   // this grid has left), and wait for every earlier grid to finish, with its
-  // memory visible, before touching any input or output.
+  // memory visible, before reading any input into the SM or writing any
+  // output (the L2 prefetch hints below are issued before the wait).
   asm volatile("griddepcontrol.launch_dependents;");
   GroupTab tab = {nullptr, nullptr, p.row_offs, p.offs};
   if (!is_grouped(kMode) && threadIdx.x == kProducerWarp * 32) {
