@@ -126,6 +126,7 @@ struct Tile {
   int32_t rows;     // rows of the tile that belong to it (grouped mode), else 128
   int32_t cont;     // grouped: bit 0 = previous tile of this CTA is the one above in
                     // the same column strip, bit 1 = next tile is the one below
+  int32_t next_rows;  // grouped: rows of the tile below in the strip (when cont bit 1)
   uint8_t* s0_dst;  // 512-byte blocked tile for dim0 scales
   uint8_t* s1_dst;  // 512-byte blocked tile for dim1 scales (null: scattered)
 };
@@ -210,6 +211,7 @@ template <int kMode>
 __device__ __forceinline__ Tile get_tile(const Params& p, const GroupTab& tab, int64_t t) {
   Tile T;
   T.cont = 0;
+  T.next_rows = 0;
   {
     const int32_t tm = static_cast<int32_t>(t / p.n_kt);
     const int32_t tk = static_cast<int32_t>(t - static_cast<int64_t>(tm) * p.n_kt);
@@ -321,6 +323,7 @@ struct GroupCursor {
     T.m0 = static_cast<int32_t>(m0);
     T.k0 = static_cast<int32_t>(tk * kTile);
     T.rows = static_cast<int32_t>(left < kTile ? left : kTile);
+    T.next_rows = static_cast<int32_t>(left - kTile < kTile ? left - kTile : kTile);
     T.cont = kBands ? ((tm > b0 ? 1 : 0) | (tm + 1 < bend ? 2 : 0))
                     : ((tm > 0 ? 1 : 0) | (tm + 1 < n_tg ? 2 : 0));
     T.s0_dst = p.s0 + ((tr_g + tm) * p.n_kt + tk) * kScaleTile;
@@ -488,19 +491,25 @@ __device__ __forceinline__ void store_partial(uint8_t* g, const uint4& v, int lo
   }
 }
 
-// Grouped mode, whole interior tile of a column strip: rewrite the staged q1
-// rows in place onto their aligned chunks (chunk 0 completes the previous
+// Grouped mode, M % 16 == 0 (every q1 row of a tile starts at the same offset
+// delta != 0 inside a 16-byte chunk), a whole tile whose tile above was this
+// CTA's previous one: rewrite the staged q1 rows in place onto their aligned
+// chunks [m0 - delta, m0 - delta + 128) (chunk 0 completes the previous
 // tile's partial last chunk from the carried bytes), so that each row is one
 // 16-byte aligned 128-byte TMA box.  The row's raw last 16 bytes become the
-// carried chunk of the next tile.  One lane per q1 row: store warp sw_idx owns
-// staging rows 16*sw_idx .. +15 of both halves (the rows it stores by TMA);
-// each 8-lane phase takes eight consecutive staging rows of one half, whose
-// swizzles differ, so the 16-byte accesses are conflict-free.  The lane loads
-// its extended row [carried chunk | 128 staged bytes] (36 words), shifts it by
-// the uniform byte offset 16 - delta (word offset by two select levels, byte
-// offset by funnel shifts) and writes it back; no lane touches another's row.
+// carried chunk of the next tile.  When the tile below is not this CTA's next
+// one (`tail`), the row's last delta bytes, which lie past the box, are stored
+// here with the fewest aligned narrow stores.  One lane per q1 row: store
+// warp sw_idx owns staging rows 16*sw_idx .. +15 of both halves (the rows it
+// stores by TMA); each 8-lane phase takes eight consecutive staging rows of
+// one half, whose swizzles differ, so the 16-byte accesses are conflict-free.
+// The lane loads its extended row [carried chunk | 128 staged bytes], shifts
+// it by the uniform byte offset 16 - delta (word offset by two select levels,
+// byte offset by funnel shifts) and writes it back; no lane touches another's
+// row.
 __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta, int sw_idx,
-                                              int lane) {
+                                              int lane, bool tail, uint8_t* q1, int64_t M,
+                                              int64_t K, int m0, int k0, const Span& sq1) {
   const int i = lane & 7, ph = lane >> 3;
   const int mrow = (2 * sw_idx + (ph >> 1)) * 8 + i;   // staging row, 16*sw_idx .. +15
   const int h = ph & 1;                                  // even / odd q1 half
@@ -508,7 +517,7 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
   uint8_t* srow = q1s + h * kQ1Half + mrow * 128;
   const int sw = mrow & 7;
   uint8_t* cslot = carry + c * 16;
-  uint32_t e[36];
+  uint32_t e[40];
   {
     const uint4 v = *reinterpret_cast<const uint4*>(cslot);
     e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
@@ -518,14 +527,15 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
     const uint4 v = *reinterpret_cast<const uint4*>(srow + ((k ^ sw) << 4));
     e[4 + 4 * k] = v.x; e[5 + 4 * k] = v.y; e[6 + 4 * k] = v.z; e[7 + 4 * k] = v.w;
   }
+  e[36] = e[37] = e[38] = e[39] = 0u;
   const int s = 16 - delta;                              // 1 .. 15
   const bool q1b = (s >> 2) & 1, q2b = (s >> 2) & 2;
   const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
-  uint32_t f[35], g[33];
+  uint32_t f[39], g[37];
 #pragma unroll
-  for (int t = 0; t < 35; ++t) f[t] = q1b ? e[t + 1] : e[t];
+  for (int t = 0; t < 39; ++t) f[t] = q1b ? e[t + 1] : e[t];
 #pragma unroll
-  for (int t = 0; t < 33; ++t) g[t] = q2b ? f[t + 2] : f[t];
+  for (int t = 0; t < 37; ++t) g[t] = q2b ? f[t + 2] : f[t];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     uint4 o;
@@ -536,6 +546,78 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
     *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = o;
   }
   *reinterpret_cast<uint4*>(cslot) = make_uint4(e[32], e[33], e[34], e[35]);
+  const int64_t kk = static_cast<int64_t>(k0) + c;
+  if (tail && kk < K) {
+    uint4 o;
+    o.x = __funnelshift_r(g[32], g[33], r);
+    o.y = __funnelshift_r(g[33], g[34], r);
+    o.z = __funnelshift_r(g[34], g[35], r);
+    o.w = __funnelshift_r(g[35], g[36], r);
+    uint8_t* gp = q1 + (kk * M + m0 - delta + 128);      // 16-byte aligned
+    if (in_span(sq1, gp, delta)) store_partial(gp, o, 0, delta);
+  }
+}
+
+// Grouped mode, M % 16 == 0, a whole tile that starts a CTA's run in a strip
+// of a misaligned group (the tile above is another CTA's, or another group's)
+// while the tile below is this CTA's next one, with at least 16 - delta rows:
+// the rows leave as boxes one chunk later, [m0 - delta + 16, m0 - delta +
+// 144), which the first 16 - delta bytes of the tile below complete (its
+// staging is in hand).  The rows' first 16 - delta bytes, in the chunk shared
+// with the tile above, are stored here with the fewest aligned narrow stores;
+// the tile below's own box writes its first chunk, the same bytes as this
+// box's last chunk, again.  The raw last 16 bytes of each row become the
+// carried chunk of the tile below.  Lane mapping as in shift_q1_rows.
+__device__ __forceinline__ void shift_q1_rows_next(uint8_t* q1s, const uint8_t* q1s_next,
+                                                   uint8_t* carry, int delta, int sw_idx,
+                                                   int lane, uint8_t* q1, int64_t M, int64_t K,
+                                                   int m0, int k0, const Span& sq1) {
+  const int i = lane & 7, ph = lane >> 3;
+  const int mrow = (2 * sw_idx + (ph >> 1)) * 8 + i;
+  const int h = ph & 1;
+  const int c = 2 * mrow + h;
+  uint8_t* srow = q1s + h * kQ1Half + mrow * 128;
+  const int sw = mrow & 7;
+  uint32_t e[40];
+  e[0] = e[1] = e[2] = e[3] = 0u;                        // no bytes before the tile
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = *reinterpret_cast<const uint4*>(srow + ((k ^ sw) << 4));
+    e[4 + 4 * k] = v.x; e[5 + 4 * k] = v.y; e[6 + 4 * k] = v.z; e[7 + 4 * k] = v.w;
+  }
+  {
+    const uint4 v = *reinterpret_cast<const uint4*>(q1s_next + h * kQ1Half + mrow * 128 +
+                                                    ((0 ^ sw) << 4));
+    e[36] = v.x; e[37] = v.y; e[38] = v.z; e[39] = v.w;
+  }
+  const int s = 16 - delta;                              // 1 .. 15
+  const bool q1b = (s >> 2) & 1, q2b = (s >> 2) & 2;
+  const uint32_t r = 8u * static_cast<uint32_t>(s & 3);
+  uint32_t f[39], g[37];
+#pragma unroll
+  for (int t = 0; t < 39; ++t) f[t] = q1b ? e[t + 1] : e[t];
+#pragma unroll
+  for (int t = 0; t < 37; ++t) g[t] = q2b ? f[t + 2] : f[t];
+  const int64_t kk = static_cast<int64_t>(k0) + c;
+  if (kk < K) {                                          // chunk 0: bytes [delta, 16)
+    uint4 o;
+    o.x = __funnelshift_r(g[0], g[1], r);
+    o.y = __funnelshift_r(g[1], g[2], r);
+    o.z = __funnelshift_r(g[2], g[3], r);
+    o.w = __funnelshift_r(g[3], g[4], r);
+    uint8_t* gp = q1 + (kk * M + m0 - delta);            // 16-byte aligned
+    if (in_span(sq1, gp + delta, 16 - delta)) store_partial(gp, o, delta, 16);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {                          // chunks 1 .. 8
+    uint4 o;
+    o.x = __funnelshift_r(g[4 * k + 4], g[4 * k + 5], r);
+    o.y = __funnelshift_r(g[4 * k + 5], g[4 * k + 6], r);
+    o.z = __funnelshift_r(g[4 * k + 6], g[4 * k + 7], r);
+    o.w = __funnelshift_r(g[4 * k + 7], g[4 * k + 8], r);
+    *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = o;
+  }
+  *reinterpret_cast<uint4*>(carry + c * 16) = make_uint4(e[32], e[33], e[34], e[35]);
 }
 
 // Grouped mode, other tiles (strip ends, partial tiles, the first tile of a
@@ -843,23 +925,44 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
         // Grouped: store warp sw owns rows 16*sw .. 16*sw+15 of each q1 half.
         // A whole 128-row tile whose q1 rows are 16-byte aligned at a common
         // offset leaves by TMA (one 16-row box per half and warp), shifted
-        // onto the aligned chunks when that offset is not 0 (which needs the
-        // carried chunk of the tile above and hands its own last chunk to the
-        // tile below).  Other tiles (strip ends, partial tiles, odd M) are
-        // stored piecewise.
+        // onto the aligned chunks when that offset is not 0:
+        //   - the tile above was this CTA's: boxes from its carried chunk (the
+        //     row's last bytes are carried on, or stored narrow at a run end);
+        //   - a run's first tile in the strip: boxes one chunk later, completed
+        //     by the first bytes of the tile below (this CTA's next one), and
+        //     the row's first bytes stored narrow.
+        // Other tiles (partial tiles, a lone tile, odd M) are stored piecewise.
+        // Measured at 16640 x 5120, G = 4 (three misaligned groups): the
+        // run's first and last tiles as boxes cut the piecewise tiles from 3.2
+        // to 1.1 per CTA, 62.9 -> 62.5 us (65536 x 5120, G = 16: 256 -> 245).
         const bool cont_prev = (T.cont & 1) && t > first;
         const bool cont_next = (T.cont & 2) && t + 1 < end;
         const int delta = T.m0 & 15;
-        const bool q1_box =
-            p.q1_tma && T.rows == kTile && (delta == 0 || (cont_prev && cont_next));
-        if (q1_box) {
-          if (delta != 0) shift_q1_rows(q1s, smem + kOffCarry, delta, sw, lane);
+        const bool full = p.q1_tma && T.rows == kTile;
+        // a run's first tile in a misaligned strip: boxes one chunk later
+        const bool box_next = full && delta != 0 && !cont_prev && cont_next &&
+                              T.next_rows >= 16 - delta;
+        if (box_next || (full && (delta == 0 || cont_prev))) {
+          int x = T.m0 - delta;
+          if (box_next) {
+            // the tile below is this CTA's next one: wait for its staging
+            const int o2 = static_cast<int>((it + 1) % kStaging);
+            const uint32_t ph2 = static_cast<uint32_t>(((it + 1) / kStaging) & 1);
+            const bool ok2 = mbar_wait(&sfull[o2], ph2, abort_flag);
+            if (!__all_sync(0xffffffffu, ok2)) break;
+            shift_q1_rows_next(q1s, smem + kOffQ1 + o2 * kQBytes, smem + kOffCarry, delta, sw,
+                               lane, p.q1, p.M, p.K, T.m0, T.k0, p.sp_q1);
+            x += 16;
+          } else if (delta != 0) {
+            shift_q1_rows(q1s, smem + kOffCarry, delta, sw, lane, !cont_next, p.q1, p.M, p.K,
+                          T.m0, T.k0, p.sp_q1);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           const int y = (T.k0 >> 1) + kQ1GroupBoxRows * sw;
           if (lane == 0 && 2 * static_cast<int64_t>(y) < p.K) {
-            tma_store_2d(&tm_q1e, T.m0 - delta, y, q1s + sw * kQ1GroupBoxRows * 128);
-            tma_store_2d(&tm_q1o, T.m0 - delta, y, q1s + kQ1Half + sw * kQ1GroupBoxRows * 128);
+            tma_store_2d(&tm_q1e, x, y, q1s + sw * kQ1GroupBoxRows * 128);
+            tma_store_2d(&tm_q1o, x, y, q1s + kQ1Half + sw * kQ1GroupBoxRows * 128);
           }
         } else {
           copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows, cont_prev,
