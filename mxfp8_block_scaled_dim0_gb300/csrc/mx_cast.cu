@@ -70,9 +70,8 @@ constexpr int kOffIn = 0;
 constexpr int kOffQ1 = kOffIn + kStages * kInBytes;
 constexpr int kOffS0 = kOffQ1 + kStaging * kQBytes;
 constexpr int kOffS1 = kOffS0 + kStaging * kScaleTile;
-constexpr int kOffCarry = kOffS1 + kStaging * kScaleTile;   // grouped: 128 x 16 B
 // group table in smem up to kMaxSmemGroups groups (mx_kernels.h)
-constexpr int kOffGTab = kOffCarry + kTile * 16;
+constexpr int kOffGTab = kOffS1 + kStaging * kScaleTile;
 constexpr int kGTabBytes = ((2 * kMaxSmemGroups + 1) * 4 + 127) / 128 * 128;
 constexpr int kOffBar = kOffGTab + kGTabBytes;
 constexpr int kNumBars = 2 * kStages + 2 * kStaging + 1;   // + the diagnostic stall barrier
@@ -507,7 +506,7 @@ __device__ __forceinline__ void store_partial(uint8_t* g, const uint4& v, int lo
 // it by the uniform byte offset 16 - delta (word offset by two select levels,
 // byte offset by funnel shifts) and writes it back; no lane touches another's
 // row.
-__device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int delta, int sw_idx,
+__device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint4& carry, int delta, int sw_idx,
                                               int lane, bool tail, uint8_t* q1, int64_t M,
                                               int64_t K, int m0, int k0, const Span& sq1) {
   const int i = lane & 7, ph = lane >> 3;
@@ -516,12 +515,8 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
   const int c = 2 * mrow + h;                            // q1 row within the tile
   uint8_t* srow = q1s + h * kQ1Half + mrow * 128;
   const int sw = mrow & 7;
-  uint8_t* cslot = carry + c * 16;
   uint32_t e[40];
-  {
-    const uint4 v = *reinterpret_cast<const uint4*>(cslot);
-    e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
-  }
+  e[0] = carry.x; e[1] = carry.y; e[2] = carry.z; e[3] = carry.w;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint4 v = *reinterpret_cast<const uint4*>(srow + ((k ^ sw) << 4));
@@ -545,7 +540,7 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
     o.w = __funnelshift_r(g[4 * k + 3], g[4 * k + 4], r);
     *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = o;
   }
-  *reinterpret_cast<uint4*>(cslot) = make_uint4(e[32], e[33], e[34], e[35]);
+  carry = make_uint4(e[32], e[33], e[34], e[35]);
   const int64_t kk = static_cast<int64_t>(k0) + c;
   if (tail && kk < K) {
     uint4 o;
@@ -569,7 +564,7 @@ __device__ __forceinline__ void shift_q1_rows(uint8_t* q1s, uint8_t* carry, int 
 // box's last chunk, again.  The raw last 16 bytes of each row become the
 // carried chunk of the tile below.  Lane mapping as in shift_q1_rows.
 __device__ __forceinline__ void shift_q1_rows_next(uint8_t* q1s, const uint8_t* q1s_next,
-                                                   uint8_t* carry, int delta, int sw_idx,
+                                                   uint4& carry, int delta, int sw_idx,
                                                    int lane, uint8_t* q1, int64_t M, int64_t K,
                                                    int m0, int k0, const Span& sq1) {
   const int i = lane & 7, ph = lane >> 3;
@@ -617,7 +612,7 @@ __device__ __forceinline__ void shift_q1_rows_next(uint8_t* q1s, const uint8_t* 
     o.w = __funnelshift_r(g[4 * k + 7], g[4 * k + 8], r);
     *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = o;
   }
-  *reinterpret_cast<uint4*>(carry + c * 16) = make_uint4(e[32], e[33], e[34], e[35]);
+  carry = make_uint4(e[32], e[33], e[34], e[35]);
 }
 
 // Grouped mode, other tiles (strip ends, partial tiles, the first tile of a
@@ -633,7 +628,7 @@ __device__ __forceinline__ void shift_q1_rows_next(uint8_t* q1s, const uint8_t* 
 // aligned 8 / 4 / 2 / 1-byte stores.  When the tile below follows in this
 // CTA, the last chunk is not stored: it is completed there from the carried
 // raw last 16 bytes of this row.
-__device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, uint8_t* q1,
+__device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint4& carry, uint8_t* q1,
                                             int64_t M, int64_t K, int m0, int k0, int len,
                                             bool cont_prev, bool cont_next, int sw_idx, int lane,
                                             const Span& sq1) {
@@ -645,14 +640,12 @@ __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, 
   if (kk >= K) return;
   const uint8_t* srow = q1s + h * kQ1Half + mrow * 128;
   const int sw = mrow & 7;
-  uint8_t* cslot = carry + c * 16;
   const int64_t A = kk * M + m0;                         // byte offset of the row segment
   const int delta = static_cast<int>(A & 15);
   uint8_t* g = q1 + (A - delta);                         // its first aligned chunk
   uint32_t e[44];
   if (cont_prev) {
-    const uint4 v = *reinterpret_cast<const uint4*>(cslot);
-    e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
+    e[0] = carry.x; e[1] = carry.y; e[2] = carry.z; e[3] = carry.w;
   } else {
     e[0] = e[1] = e[2] = e[3] = 0u;
   }
@@ -692,7 +685,7 @@ __device__ __forceinline__ void copy_out_q1(const uint8_t* q1s, uint8_t* carry, 
       else store_partial(g + 16 * j, v, b_lo, b_hi);
     }
   }
-  if (cont_next) *reinterpret_cast<uint4*>(cslot) = make_uint4(e[32], e[33], e[34], e[35]);
+  if (cont_next) carry = make_uint4(e[32], e[33], e[34], e[35]);
 }
 
 // One warp builds the grouped mode's group table from the offsets: it
@@ -914,6 +907,9 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     typename ItType<kMode>::T it = 0;
     GroupCursor<kMode == kModeGroupedBands> cur;
     if (is_grouped(kMode)) cur.init(p, tab, first, run_len);
+    // grouped: the raw last 16 bytes of this lane's q1 row of the previous
+    // tile (a lane keeps the same row of every tile)
+    uint4 carry = make_uint4(0u, 0u, 0u, 0u);
     for (int64_t t = first; t < end; t += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
@@ -950,11 +946,11 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
             const uint32_t ph2 = static_cast<uint32_t>(((it + 1) / kStaging) & 1);
             const bool ok2 = mbar_wait(&sfull[o2], ph2, abort_flag);
             if (!__all_sync(0xffffffffu, ok2)) break;
-            shift_q1_rows_next(q1s, smem + kOffQ1 + o2 * kQBytes, smem + kOffCarry, delta, sw,
+            shift_q1_rows_next(q1s, smem + kOffQ1 + o2 * kQBytes, carry, delta, sw,
                                lane, p.q1, p.M, p.K, T.m0, T.k0, p.sp_q1);
             x += 16;
           } else if (delta != 0) {
-            shift_q1_rows(q1s, smem + kOffCarry, delta, sw, lane, !cont_next, p.q1, p.M, p.K,
+            shift_q1_rows(q1s, carry, delta, sw, lane, !cont_next, p.q1, p.M, p.K,
                           T.m0, T.k0, p.sp_q1);
           }
           fence_proxy_async_smem();
@@ -965,7 +961,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
             tma_store_2d(&tm_q1o, x, y, q1s + kQ1Half + sw * kQ1GroupBoxRows * 128);
           }
         } else {
-          copy_out_q1(q1s, smem + kOffCarry, p.q1, p.M, p.K, T.m0, T.k0, T.rows, cont_prev,
+          copy_out_q1(q1s, carry, p.q1, p.M, p.K, T.m0, T.k0, T.rows, cont_prev,
                       cont_next, sw, lane, p.sp_q1);
         }
       } else if (kDim1 && lane == 0) {
