@@ -41,6 +41,8 @@
 // device word.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "mx_common.cuh"
 #include "mx_kernels.h"
 
@@ -48,6 +50,9 @@ namespace mx {
 
 // Device-side watchdog word: set when any CTA gave up waiting.
 __device__ int g_watchdog = 0;
+// Claim counters (kClaim launches), one per stream in use (claim_counter).
+constexpr int kClaimSlots = 64;
+__device__ unsigned int g_claims[kClaimSlots];
 
 namespace {
 
@@ -59,6 +64,12 @@ constexpr int kQ1Half = 64 * 128;           // even / odd columns of a q1 tile
 constexpr int kScaleTile = 512;
 constexpr int kStages = 3;                 // input ring depth
 constexpr int kStaging = 6;                // q1 / scale staging buffers
+// claim schedule (mx_cast_kernel): the last kClaimRounds rounds are claimed,
+// for launches of at least kClaimMinRounds rounds (fewer: static).  At
+// 16384^2 (108 rounds) it takes 165.6 -> 164.6 us; claiming 6, 10 or 16
+// rounds measured alike; at 8192^2 (27 rounds) it cost 0.65 us.
+constexpr int64_t kClaimRounds = 6;
+constexpr int64_t kClaimMinRounds = 32;
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kProducerWarp = kComputeWarps;
@@ -77,7 +88,10 @@ constexpr int kOffBar = kOffGTab + kGTabBytes;
 constexpr int kNumBars = 2 * kStages + 2 * kStaging + 1;   // + the diagnostic stall barrier
 constexpr int kQ1GroupBoxRows = static_cast<int>(kQ1BoxRowsGrouped);  // grouped: per-warp q1 box rows
 constexpr int kOffFlag = kOffBar + kNumBars * 8;
-constexpr int kSmemUsed = kOffFlag + 16;   // flag: abort (+0), bad group offsets (+4)
+// claim schedule: the tile of each input stage and staging buffer, as the
+// producer chose it (-1: no more tiles)
+constexpr int kOffIds = kOffFlag + 16;     // flag: abort (+0), bad group offsets (+4)
+constexpr int kSmemUsed = kOffIds + (kStages + kStaging) * 8;
 constexpr int kStatusBadGroups = -5;        // MX_ERR_GROUPS
 constexpr int kSmemBytes = kSmemUsed + 1024;
 
@@ -163,6 +177,9 @@ struct Params {
   // stall_at, -1 in normal use
   int64_t stall_at;
   uint64_t stall_ns;
+  // 2D / 3D modes with the claim schedule: this launch's tile counter (one
+  // word of g_claims, zero between launches)
+  unsigned int* claims;
 };
 
 // Group table of the grouped mode: tr[g] = padded tile-rows before group g
@@ -731,10 +748,19 @@ __device__ __forceinline__ int64_t warp_group_table(const Params& p, int32_t* tr
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int kMode>
+// kClaim (2D / 3D modes, launches of kClaimMinRounds rounds or more): the
+// last kClaimRounds rounds of tiles are not dealt out in advance but claimed
+// from a counter, one tile ahead, so that the CTAs that run fast take more of
+// them and all finish close together.  Every CTA makes exactly one claim that
+// finds no tile, so a launch makes a known number of claims, and the CTA that
+// makes the last one resets the counter: nothing runs after the final
+// barrier, and the next launch on the stream (which claims only after this
+// one has completed) finds it at zero.
+template <int kMode, bool kClaim>
 __global__ void __launch_bounds__(threads_of(kMode), 1)
     mx_cast_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q1e,
                    const __grid_constant__ CUtensorMap tm_q1o, const Params p) {
+  static_assert(!(kClaim && is_grouped(kMode)), "the grouped schedule is static");
   constexpr bool kDim0 = has_dim0(kMode);
   constexpr bool kDim1 = has_dim1(kMode);
   constexpr bool kTmaQ1 = kDim1 && !is_grouped(kMode);
@@ -747,6 +773,8 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
   uint64_t* sfull = bars + 2 * kStages;       // [kStaging] staging written
   uint64_t* sempty = sfull + kStaging;        // [kStaging] staging drained
   uint64_t* stall_bar = sempty + kStaging;    // diagnostic: never completed
+  int64_t* ids_in = reinterpret_cast<int64_t*>(smem + kOffIds);   // claim schedule: [kStages]
+  int64_t* ids_st = ids_in + kStages;                                // [kStaging]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
 
   const int warp = threadIdx.x >> 5;
@@ -877,6 +905,43 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       typename ItType<kMode>::T it = 0;
       GroupCursor<kMode == kModeGroupedBands> cur;
       if (is_grouped(kMode)) cur.init(p, tab, first, run_len);
+      if (kClaim) {
+        const int64_t g = gridDim.x;
+        const int64_t n_static = p.n_tiles / g - kClaimRounds;   // whole rounds dealt out
+        const int64_t n_claims = p.n_tiles - n_static * g + g;
+        int64_t next = blockIdx.x;
+        for (;; ++it) {
+          const int s = static_cast<int>(it % kStages);
+          const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+          if (kDiagStall && static_cast<int64_t>(it) == p.stall_at && blockIdx.x == 0) {
+            mbar_wait(stall_bar, 0u, abort_flag, p.stall_ns);   // as in the static loop
+            break;
+          }
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
+          const int64_t t = next;
+          if (t >= p.n_tiles) {                   // tell the other roles: no more tiles
+            ids_in[s] = -1;
+            mbar_arrive(&full[s]);
+            break;
+          }
+          ids_in[s] = t;
+          const Tile T = get_tile<kMode>(p, tab, t);
+          uint8_t* dst = smem + kOffIn + s * kInBytes;
+          mbar_arrive_expect_tx(&full[s], kInBytes);
+          tma_load_2d(dst, &tm_x, T.k0, T.m0, &full[s]);
+          tma_load_2d(dst + kHalfBytes, &tm_x, T.k0 + 64, T.m0, &full[s]);
+          issued = static_cast<int64_t>(it) + 1;
+          // the next tile: dealt out, or claimed (after this tile's loads are
+          // on their way, so that the claim's latency overlaps them)
+          if (static_cast<int64_t>(it) + 1 < n_static) {
+            next = blockIdx.x + g * (static_cast<int64_t>(it) + 1);
+          } else {
+            const unsigned int v = atomicAdd(p.claims, 1u);
+            if (static_cast<int64_t>(v) == n_claims - 1) atomicExch(p.claims, 0u);
+            next = n_static * g + static_cast<int64_t>(v);
+          }
+        }
+      } else
       for (int64_t t = first; t < end; t += step, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
@@ -910,11 +975,13 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     // grouped: the raw last 16 bytes of this lane's q1 row of the previous
     // tile (a lane keeps the same row of every tile)
     uint4 carry = make_uint4(0u, 0u, 0u, 0u);
-    for (int64_t t = first; t < end; t += step, ++it) {
+    for (int64_t t0 = first; kClaim || t0 < end; t0 += step, ++it) {
       const int o = static_cast<int>(it % kStaging);
       const uint32_t ph = static_cast<uint32_t>((it / kStaging) & 1);
       const bool ok = mbar_wait(&sfull[o], ph, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
+      const int64_t t = kClaim ? ids_st[o] : t0;
+      if (kClaim && t < 0) break;
       const Tile T = role_tile<kMode>(p, tab, t, cur);
       uint8_t* q1s = smem + kOffQ1 + o * kQBytes;
       if (is_grouped(kMode)) {
@@ -1005,7 +1072,7 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
     typename ItType<kMode>::T it = 0;
     GroupCursor<kMode == kModeGroupedBands> cur;
     if (is_grouped(kMode)) cur.init(p, tab, first, run_len);
-    for (int64_t t = first; t < end; t += step, ++it) {
+    for (int64_t t0 = first; kClaim || t0 < end; t0 += step, ++it) {
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
       const int o = static_cast<int>(it % kStaging);
@@ -1013,6 +1080,15 @@ __global__ void __launch_bounds__(threads_of(kMode), 1)
       bool ok = mbar_wait(&full[s], ph, abort_flag);
       ok = ok && mbar_wait(&sempty[o], oph ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
+      const int64_t t = kClaim ? ids_in[s] : t0;
+      if (kClaim && t < 0) {                   // no more tiles: pass it on to the store warp
+        if (lane == 0) {
+          ids_st[o] = -1;
+          mbar_arrive(&sfull[o]);
+        }
+        break;
+      }
+      if (kClaim && lane == 0 && warp == 0) ids_st[o] = t;
 
       const Tile T = role_tile<kMode>(p, tab, t, cur);
       const uint8_t* in = smem + kOffIn + s * kInBytes;
@@ -1111,11 +1187,11 @@ int set_smem(const void* fn) {
   return e == cudaSuccess ? 0 : static_cast<int>(e);
 }
 
-template <int kMode>
+template <int kMode, bool kClaim = false>
 int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t stream) {
   static DeviceCache smem_attr;
-  const int attr_rc =
-      smem_attr.get([] { return set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode>)); });
+  const int attr_rc = smem_attr.get(
+      [] { return set_smem(reinterpret_cast<const void*>(&mx_cast_kernel<kMode, kClaim>)); });
   if (attr_rc != 0) return attr_rc;
   // Launched as a programmatic dependent of the previous work in the stream:
   // when that is a cast kernel (which triggers its dependents early), this
@@ -1131,11 +1207,71 @@ int launch(const CastMaps& maps, const Params& prm, int grid, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return static_cast<int>(cudaLaunchKernelEx(&cfg, mx_cast_kernel<kMode>, maps.x, maps.q1e, maps.q1o,
-                                             prm));
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, mx_cast_kernel<kMode, kClaim>, maps.x, maps.q1e,
+                                             maps.q1o, prm));
 }
 
 }  // namespace
+
+// The claim counter for a launch on `stream` of the current device, or null
+// for the static schedule.  Each (device, stream) in use keeps one word of
+// g_claims: launches on one stream run one after another (each claims only
+// after the previous grid has completed), while launches on different streams
+// may overlap and so must not share a counter.  Null when the stream is being
+// captured into a graph (a graph may be launched on any stream, so its
+// counter could be shared), for cudaStreamPerThread (one handle for many
+// streams), when the slots are all taken, or when the symbol cannot be found.
+// A stream destroyed while a cast is still running on it must not be replaced
+// by a new stream that launches casts before that cast has finished (the new
+// stream could get the same handle and counter).
+unsigned int* claim_counter(cudaStream_t stream) {
+  if (stream == cudaStreamPerThread) return nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= DeviceCache::kMaxDevices) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  struct Slots {
+    unsigned int* base = nullptr;
+    cudaStream_t stream[kClaimSlots] = {};
+    int n = 0;
+  };
+  static Slots slots[DeviceCache::kMaxDevices];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  Slots& d = slots[dev];
+  if (!d.base) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_claims) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    d.base = static_cast<unsigned int*>(a);
+  }
+  for (int i = 0; i < d.n; ++i)
+    if (d.stream[i] == stream) return d.base + i;
+  if (d.n == kClaimSlots) return nullptr;
+  d.stream[d.n] = stream;
+  return d.base + d.n++;
+}
+
+// Launch a 2D / 3D mode with the claim schedule when the launch is long
+// enough and a counter is free, else with the static one.
+template <int kMode>
+int launch_tiles(const CastMaps& maps, Params prm, int grid, cudaStream_t stream) {
+  if (prm.n_tiles / grid >= kClaimMinRounds) {
+    prm.claims = claim_counter(stream);
+    if (prm.claims) return launch<kMode, true>(maps, prm, grid, stream);
+  }
+  prm.claims = nullptr;
+  return launch<kMode, false>(maps, prm, grid, stream);
+}
 
 // Bytes of a blocked scale matrix (R x C scales).
 uint64_t blk_bytes(int64_t R, int64_t C) {
@@ -1166,9 +1302,9 @@ int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s
   prm.sp_s1 = make_span(s1, blk_bytes(K, M / 32));
   const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
   if (grid <= 0) return 0;
-  if (dim0 && dim1) return launch<kModeFused2D>(maps, prm, grid, stream);
-  return dim0 ? launch<kModeDim0>(maps, prm, grid, stream)
-              : launch<kModeDim1>(maps, prm, grid, stream);
+  if (dim0 && dim1) return launch_tiles<kModeFused2D>(maps, prm, grid, stream);
+  return dim0 ? launch_tiles<kModeDim0>(maps, prm, grid, stream)
+              : launch_tiles<kModeDim1>(maps, prm, grid, stream);
 }
 
 int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* q0,
@@ -1199,9 +1335,9 @@ int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, v
   prm.sp_s1 = make_span(s1, static_cast<uint64_t>(E) * prm.s1_expert_bytes);
   const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
   if (grid <= 0) return 0;
-  if (dim0 && dim1) return launch<kModeExperts01>(maps, prm, grid, stream);
-  return dim0 ? launch<kModeExperts0>(maps, prm, grid, stream)
-              : launch<kModeExperts>(maps, prm, grid, stream);
+  if (dim0 && dim1) return launch_tiles<kModeExperts01>(maps, prm, grid, stream);
+  return dim0 ? launch_tiles<kModeExperts0>(maps, prm, grid, stream)
+              : launch_tiles<kModeExperts>(maps, prm, grid, stream);
 }
 
 int launch_cast_grouped(const CastMaps& maps, int64_t M, int64_t K, const int32_t* offs, int G,
@@ -1280,6 +1416,12 @@ int read_watchdog(int* out, bool clear) {
   if (clear && v) {
     const int z = 0;
     e = cudaMemcpyToSymbol(g_watchdog, &z, sizeof(int));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    // A launch that gave up may have left its claim counter short of its
+    // reset: clear them all (the caller clears the watchdog with no cast in
+    // flight).
+    static const unsigned int zeros[kClaimSlots] = {};
+    e = cudaMemcpyToSymbol(g_claims, zeros, sizeof(zeros));
     if (e != cudaSuccess) return static_cast<int>(e);
   }
   *out = v;

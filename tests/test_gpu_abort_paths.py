@@ -58,6 +58,28 @@ def _after_abort():
     assert mx.mx_watchdog(clear=True) == 0
 
 
+@pytest.mark.parametrize("at", [0, 27])
+def test_claimed_cast_abort_path_then_exact(at):
+    """A launch long enough for the claim schedule (8192 x 10240: 33 rounds,
+    the last six claimed): CTA 0 gives up before its first tile (at = 0) or
+    at its first claimed tile (at = 27; its first claim, made with every other
+    CTA's first, always finds a tile).  It never makes its last claim, so the
+    launch's counter is not reset by the kernel; clearing the watchdog resets
+    it, and the next launch on the stream is byte-exact."""
+    _fresh()
+    x = W.normal((8192, 10240), 12)
+    xb = x.cuda()
+    mx.mx_selftest_arm_stall(at, 20_000_000)
+    mx.cast_dim0_dim1(xb)
+    _after_abort()
+    q0, s0, q1, s1 = mx.cast_dim0_dim1(xb)
+    torch.cuda.synchronize()
+    want = oracle.cast_dim0_dim1_blocked(W.bf16_bits(x))
+    for got, ref in zip((q0, s0, q1, s1), want):
+        assert np.array_equal(got.cpu().numpy().ravel(), np.asarray(ref).ravel())
+    assert mx.mx_watchdog(clear=True) == 0
+
+
 @pytest.mark.parametrize("at", [0, 2])
 def test_fused_cast_abort_path_then_exact(at):
     _fresh()
