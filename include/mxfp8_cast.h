@@ -81,6 +81,33 @@ enum {
 int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk, void* q1,
                       void* s1_blk, void* stream);
 
+/* mx_cast_dim0_dim1 for callers that must not allocate device memory, with
+ * its one piece of scratch in device memory reserved when the library is
+ * loaded.  The pages have no counterpart: this is an entry point of this
+ * library only.
+ *
+ * Who needs it: a process whose device memory is handed out by a caching
+ * allocator that reserved it up front (a training or serving framework),
+ * where an allocation from outside the pool can fail for lack of memory or
+ * fragment it; and code that must not risk the device-wide synchronisation
+ * an allocation can bring.  None of the entry points here allocate; this one
+ * also keeps no per-stream state on the host: its scratch is one fixed
+ * array instead of mx_cast_dim0_dim1's counter per stream.
+ *
+ * Arguments, layouts, output and errors as mx_cast_dim0_dim1, byte for byte.
+ * The scratch is 256 bytes (64 words) of device memory, held by every GPU
+ * that loads the library until the process exits; a call needs one word
+ * (its tile-claim counter, for launches of 32 rounds of tiles or more), and
+ * a call that would need more than 64 words is refused with MX_ERR_SHAPE.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Each call
+ * clears the word it uses on the stream before its kernel.  All calls share
+ * the array: calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on it and give wrong output; order them on one
+ * stream or with events. */
+int mx_cast_dim0_dim1_noalloc(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk,
+                              void* q1, void* s1_blk, void* stream);
+
 /* dim1 cast only (the column-major copy and its blocked scales), as split out
  * of the fused kernel in the same pull request's follow-up (dim1 logic in its
  * own kernel).  Arguments as in mx_cast_dim0_dim1. */

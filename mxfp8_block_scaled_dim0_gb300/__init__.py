@@ -38,7 +38,7 @@ ABI_SYMBOLS = (
     "mx_3d_dim0_scale_bytes", "mx_cast_tensorwise", "mx_cast_rowwise", "mx_bounds_check",
     "mx_selftest_bounds",
     "mx_strerror", "mx_last_cuda_error", "mx_watchdog",
-    "mx_selftest_watchdog", "mx_selftest_arm_stall",
+    "mx_selftest_watchdog", "mx_selftest_arm_stall", "mx_cast_dim0_dim1_noalloc",
 )
 
 

@@ -318,6 +318,25 @@ int mx_cast_dim0_dim1(const void* x, int64_t M, int64_t K, void* q0, void* s0_bl
                                       static_cast<cudaStream_t>(stream)));
 }
 
+int mx_cast_dim0_dim1_noalloc(const void* x, int64_t M, int64_t K, void* q0, void* s0_blk,
+                              void* q1, void* s1_blk, void* stream) {
+  if (!x || !q0 || !s0_blk || !q1 || !s1_blk) return MX_ERR_NULL;
+  if (int rc = check_2d_shape(M, K)) return rc;
+  if (!aligned(x, 16) || !aligned(q0, 16) || !aligned(s0_blk, 16) || !aligned(q1, 16) ||
+      !aligned(s1_blk, 16))
+    return MX_ERR_ALIGN;
+  if (int rc = check_device({x, q0, s0_blk, q1, s1_blk})) return rc;
+  mx::CastMaps maps;
+  if (int rc = encode_cast_maps(&maps, x, M, K, q1)) return rc;
+  int sms = 0;
+  if (int rc = current_sm_count(&sms)) return rc;
+  int64_t words = 0;
+  const int rc = mx::launch_cast_2d_noalloc(maps, M, K, q0, s0_blk, q1, s1_blk, sms,
+                                            static_cast<cudaStream_t>(stream), &words);
+  if (words > mx::noalloc_scratch_words()) return MX_ERR_SHAPE;   // more scratch than reserved
+  return launch_rc(rc);
+}
+
 int mx_cast_dim1(const void* x, int64_t M, int64_t K, void* q1, void* s1_blk, void* stream) {
   if (!x || !q1 || !s1_blk) return MX_ERR_NULL;
   if (int rc = check_2d_shape(M, K)) return rc;

@@ -1307,6 +1307,84 @@ int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s
               : launch_tiles<kModeDim1>(maps, prm, grid, stream);
 }
 
+// ---- the fused cast with a fixed scratch array (mx_cast_dim0_dim1_noalloc) ----
+//
+// Scratch of mx_cast_dim0_dim1_noalloc: its tile-claim counter lives here,
+// in memory that exists from the moment the library is loaded on a GPU until
+// the process exits, so a call allocates nothing.  64 words (256 bytes)
+// are reserved; a call uses one.  The host cannot use the name of this array
+// as a device address: noalloc_scratch() asks the runtime for that address,
+// once per device, with the device current.
+constexpr int kNoAllocScratchWords = 64;
+static __device__ __align__(256) unsigned int g_noalloc_scratch[kNoAllocScratchWords];
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call for that device; null (and *rc set) if the lookup failed.
+unsigned int* noalloc_scratch(int* rc) {
+  static std::mutex mu;
+  static unsigned int* addr[DeviceCache::kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *rc = static_cast<int>(e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= DeviceCache::kMaxDevices) {
+    *rc = static_cast<int>(cudaErrorInvalidDevice);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *rc = static_cast<int>(e);
+      return nullptr;
+    }
+    addr[dev] = static_cast<unsigned int*>(ptr);
+  }
+  *rc = 0;
+  return addr[dev];
+}
+
+int launch_cast_2d_noalloc(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0,
+                           void* q1, void* s1, int num_sms, cudaStream_t stream,
+                           int64_t* scratch_words) {
+  (void)q1;   // written through maps.q1e / maps.q1o
+  Params prm = {};
+  const Stall stall = take_stall();
+  prm.stall_at = stall.at;
+  prm.stall_ns = stall.ns;
+  prm.q0 = static_cast<uint8_t*>(q0);
+  prm.M = M;
+  prm.K = K;
+  prm.n_mt = static_cast<int32_t>((M + kTile - 1) / kTile);
+  prm.n_kt = static_cast<int32_t>((K + kTile - 1) / kTile);
+  prm.n_tiles = static_cast<int64_t>(prm.n_mt) * prm.n_kt;
+  prm.s0 = static_cast<uint8_t*>(s0);
+  prm.s1 = static_cast<uint8_t*>(s1);
+  prm.sp_q0 = make_span(q0, static_cast<uint64_t>(M) * K);
+  prm.sp_s0 = make_span(s0, blk_bytes(M, K / 32));
+  prm.sp_s1 = make_span(s1, blk_bytes(K, M / 32));
+  const int grid = static_cast<int>(prm.n_tiles < num_sms ? prm.n_tiles : num_sms);
+  if (grid <= 0) return 0;
+  // Scratch this call needs: one counter when it claims tiles, else none.
+  const bool claim = prm.n_tiles / grid >= kClaimMinRounds;
+  *scratch_words = claim ? 1 : 0;
+  if (*scratch_words > kNoAllocScratchWords) return static_cast<int>(cudaErrorInvalidValue);
+  if (!claim) return launch<kModeFused2D, false>(maps, prm, grid, stream);
+  int rc = 0;
+  prm.claims = noalloc_scratch(&rc);
+  if (!prm.claims) return rc;
+  // The counter must start at zero; a call that gave up may have left it
+  // short of its reset, so clear it on the stream first.
+  cudaError_t e = cudaMemsetAsync(prm.claims, 0, sizeof(unsigned int), stream);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  return launch<kModeFused2D, true>(maps, prm, grid, stream);
+}
+
+int noalloc_scratch_words() { return kNoAllocScratchWords; }
+
 int launch_cast_experts(const CastMaps& maps, int64_t E, int64_t N, int64_t K, void* q0,
                         void* s0, void* s1, int num_sms, cudaStream_t stream) {
   const bool dim0 = q0 != nullptr;

@@ -68,6 +68,13 @@ int threads_cast();
 // q0 == nullptr: dim1 only; s1 == nullptr: dim0 only.
 int launch_cast_2d(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0, void* s1,
                    int num_sms, cudaStream_t stream);
+// The fused cast with its tile-claim counter in a fixed device array instead
+// of a per-stream counter (mx_cast_dim0_dim1_noalloc); *scratch_words is set
+// to the words of that array the call needs (0 or 1).
+int launch_cast_2d_noalloc(const CastMaps& maps, int64_t M, int64_t K, void* q0, void* s0,
+                           void* q1, void* s1, int num_sms, cudaStream_t stream,
+                           int64_t* scratch_words);
+int noalloc_scratch_words();
 // 3D weights (E, N, K) as the (E*N, K) matrix, scales blocked per expert;
 // same null conventions.  With N % 128 != 0 the scales are scattered byte by
 // byte and the caller clears the scale buffers first.
