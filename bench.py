@@ -45,6 +45,7 @@ KERNEL_SOURCES = ["mxfp8_block_scaled_dim0_gb300/csrc/mx_cast.cu",
                   "mxfp8_block_scaled_dim0_gb300/csrc/mx_common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "mx_cast_fused_16384x16384.txt")
 E2E_RUNS = 3                # timed end-to-end runs; the median is reported
+E2E_SETS = 3                # end-to-end buffer sets and streams, used in rotation
 
 
 def algorithmic_bytes(M, K):
@@ -538,27 +539,31 @@ def run_gpu(args):
 
     # End to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory, calls the cast, and copies every
-    # output back to pinned host memory.  Consecutive steps alternate between
-    # two buffer sets on two streams, so that one step's device-to-host copies
-    # overlap the next step's host-to-device copies (separate copy engines).
+    # output back to pinned host memory.  Consecutive steps rotate over
+    # E2E_SETS buffer sets on as many streams, so that the device-to-host
+    # copies of step i run while the host-to-device copies of the next steps
+    # do (separate copy engines), and the cast of step i is off the copy
+    # engines' path: with two sets, step i+2's inputs wait for step i's cast
+    # and outputs on the same stream.
     e2e = None
     if args.e2e_steps > 0:
-        streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-        host_in = [{j: sets[k][j].cpu().pin_memory() for j in R.inputs} for k in range(2)]
-        host_out = [{j: torch.empty(sets[k][j].shape, dtype=sets[k][j].dtype).pin_memory()
-                     for j in R.outputs} for k in range(2)]
+        esets = sets + [R.build(k) for k in range(len(sets), E2E_SETS)]
+        streams = [torch.cuda.Stream(dev) for _ in range(E2E_SETS)]
+        host_in = [{j: esets[k][j].cpu().pin_memory() for j in R.inputs} for k in range(E2E_SETS)]
+        host_out = [{j: torch.empty(esets[k][j].shape, dtype=esets[k][j].dtype).pin_memory()
+                     for j in R.outputs} for k in range(E2E_SETS)]
 
         def e2e_step(i):
-            k = i & 1
+            k = i % E2E_SETS
             st = streams[k]
             with torch.cuda.stream(st):
                 for j in R.inputs:
-                    sets[k][j].copy_(host_in[k][j], non_blocking=True)
-                R.call(sets[k], st)
+                    esets[k][j].copy_(host_in[k][j], non_blocking=True)
+                R.call(esets[k], st)
                 for j in R.outputs:
-                    host_out[k][j].copy_(sets[k][j], non_blocking=True)
+                    host_out[k][j].copy_(esets[k][j], non_blocking=True)
 
-        for i in range(2):
+        for i in range(E2E_SETS):
             e2e_step(i)
         torch.cuda.synchronize(dev)
         # E2E_RUNS timed runs of e2e_steps steps each; the line reports the
@@ -569,10 +574,12 @@ def run_gpu(args):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier(ws)
             a.record(streams[0])
-            streams[1].wait_event(a)
+            for s in streams[1:]:
+                s.wait_event(a)
             for i in range(args.e2e_steps):
                 e2e_step(i)
-            streams[0].wait_stream(streams[1])
+            for s in streams[1:]:
+                streams[0].wait_stream(s)
             b.record(streams[0])
             torch.cuda.synchronize(dev)
             runs.append(max_over_ranks(a.elapsed_time(b) / 1e3, ws, dev))
@@ -584,8 +591,9 @@ def run_gpu(args):
                "steps": args.e2e_steps, "ms_per_step": 1e3 * e_el / args.e2e_steps,
                "runs": [whole_job_value(nbytes, args.e2e_steps, ws, r) for r in runs],
                "timing": "median of %d timed runs of %d steps each" % (E2E_RUNS, args.e2e_steps),
-               "pipelining": "2 streams, 2 buffer sets: D2H of step i overlaps H2D of step i+1"}
-        del host_in, host_out
+               "pipelining": "%d streams, %d buffer sets: the D2H of step i overlaps the H2D of "
+                             "the next steps" % (E2E_SETS, E2E_SETS)}
+        del host_in, host_out, esets
 
     cpu = None
     if (rank == 0 and ws == 1 and args.cpu_seconds > 0 and R.name == "fused" and not args.shape
