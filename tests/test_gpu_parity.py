@@ -279,6 +279,20 @@ def test_grouped_multi_tile_runs(M, K, G, seed):
     compare_grouped(W.wide(M, K, seed, zero_frac=0.005), offs)
 
 
+@pytest.mark.parametrize("offs", [
+    [4112, 8208, 12304, 16384],     # unshifted starts at odd multiples of 16
+    [4122, 8250, 12390, 16384],     # shifted starts, boxes at 16 and 0 mod 32
+    [4164, 8282, 12462, 16384],     # the MoE workload's starts
+])
+def test_grouped_box_alignment_paths(offs):
+    """16384 x 2048, 13-14 tiles per CTA, group starts whose q1 boxes begin
+    at odd and even multiples of 16 bytes, with and without a shift: the
+    boxes from carried chunks, the run-start boxes one chunk later, the
+    narrow run-end tails and the piecewise partial tiles, every byte against
+    the oracle."""
+    compare_grouped(W.wide(16384, 2048, offs[0], zero_frac=0.005), offs)
+
+
 def test_grouped_many_groups_two_kernel_path():
     """More groups than the cast kernel tabulates itself (1024): the padded
     offsets come from the separate offsets kernel, launched before it."""
