@@ -46,6 +46,7 @@ KERNEL_SOURCES = ["mxfp8_block_scaled_dim0_gb300/csrc/mx_cast.cu",
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "mx_cast_fused_16384x16384.txt")
 E2E_RUNS = 3                # timed end-to-end runs; the median is reported
 E2E_SETS = 3                # end-to-end buffer sets and streams, used in rotation
+HOLD_CYCLES = 2_000_000     # spin ahead of a timed region (about 1 ms at 2 GHz)
 
 
 def algorithmic_bytes(M, K):
@@ -336,6 +337,16 @@ class Row:
         self.build, self.call, self.inputs, self.outputs = build, call, inputs, outputs
 
 
+def hold_gpu(torch, stream):
+    """Enqueue a short spin kernel (about a millisecond) on `stream`, ahead of
+    a timed region's start event: the GPU is then still busy while the host
+    issues the region's first launches, so the host's launch latency does not
+    sit between the two events.  The spin itself is outside the region."""
+    if hasattr(torch.cuda, "_sleep"):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(HOLD_CYCLES)
+
+
 def make_row(row, args, dev, rank):
     import torch
     import mxfp8_block_scaled_dim0_gb300 as mx
@@ -521,6 +532,7 @@ def run_gpu(args):
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize(dev)
+    hold_gpu(torch, stream)
     t_beg.record(stream)
     if graph is not None:
         for _ in range(args.steps // per_graph):
@@ -573,6 +585,7 @@ def run_gpu(args):
         for _ in range(E2E_RUNS):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier(ws)
+            hold_gpu(torch, streams[0])
             a.record(streams[0])
             for s in streams[1:]:
                 s.wait_event(a)
