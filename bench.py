@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["mxfp8_block_scaled_dim0_gb300/csrc/mx_cast.cu",
                   "mxfp8_block_scaled_dim0_gb300/csrc/mx_common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "mx_cast_fused_16384x16384.txt")
-E2E_RUNS = 3                # timed end-to-end runs; the median is reported
+E2E_RUNS = 5                # timed end-to-end runs; the median is reported
 E2E_SETS = 3                # end-to-end buffer sets and streams, used in rotation
 HOLD_CYCLES = 2_000_000     # spin ahead of a timed region (about 1 ms at 2 GHz)
 
@@ -580,7 +580,8 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         # E2E_RUNS timed runs of e2e_steps steps each; the line reports the
         # median run.  One run lasts about 40 ms at 16384^2, short enough for
-        # a one-off stall of the host link to halve a single run's figure.
+        # a stall of the host link (about 70 ms, seen in one run of three now
+        # and then) to cut a single run's figure to a third.
         runs = []
         for _ in range(E2E_RUNS):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
